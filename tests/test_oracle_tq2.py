@@ -1,0 +1,150 @@
+"""Pins of the TQ2 oracle against the pages and plain mathematics (CPU only).
+
+Each test is chosen so that a plausible slip in ``oracle/tq2.py`` (a wrong
+bit index, a code offset other than -1, a transposed operand, a dropped
+scale, a mis-read scale byte order) fails at least one of them.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import tq2
+
+
+def _page_pack_block(codes128, d_bits):
+    """One block packed the way the page's test loop does it.
+
+    ``for b in qs: c0..c3 = next_code(); b = c0 | c1<<2 | c2<<4 | c3<<6``,
+    then the f16 scale, little-endian.
+    """
+    it = iter(int(c) for c in codes128)
+    qs = []
+    for _ in range(32):
+        c0, c1, c2, c3 = next(it), next(it), next(it), next(it)
+        qs.append(c0 | (c1 << 2) | (c2 << 4) | (c3 << 6))
+    return bytes(qs) + bytes([d_bits & 0xFF, d_bits >> 8])
+
+
+def test_parse_returns_codes_in_generation_order():
+    seq = synth.lcg_codes(2 * 128 * 3)
+    blocks = b"".join(_page_pack_block(seq[i * 128:(i + 1) * 128], 0x3C00) for i in range(6))
+    codes, d = tq2.parse_aos(blocks, 3, 256)
+    assert np.array_equal(codes.reshape(-1), seq)
+    assert np.all(d == 0x3C00)
+
+
+@pytest.mark.parametrize("hot", [0, 2, 3])
+def test_one_hot_every_position(hot):
+    # all codes 1 (weight 0) except one code at position k -> W = (hot-1)*d only at k
+    d_bits, d = 0x3A00, 0.75
+    for k in range(128):
+        seq = np.ones(128, dtype=np.uint8)
+        seq[k] = hot
+        W = tq2.dequant_aos(_page_pack_block(seq, d_bits), 1, 128)
+        want = np.zeros((1, 128))
+        want[0, k] = (hot - 1) * d
+        assert np.array_equal(W, want), k
+
+
+def test_scale_bytes_little_endian_and_per_block():
+    seq = np.full(256, 2, dtype=np.uint8)              # weight = +d everywhere
+    aos = _page_pack_block(seq[:128], 0x3C00) + _page_pack_block(seq[128:], 0xC100)
+    W = tq2.dequant_aos(aos, 1, 256)
+    assert np.all(W[0, :128] == 1.0) and np.all(W[0, 128:] == -2.5)
+
+
+def test_all_codes_one_gives_zero():
+    N, K, M = 5, 384, 3
+    codes = np.ones((N, K), dtype=np.uint8)
+    d = synth.f16_bits(synth.uniform(N * 3, 1, 0.01, 0.1)).reshape(N, 3)
+    W = tq2.dequant_aos(synth.pack_aos(codes, d), N, K)
+    x = synth.random_x(M, K, 3)
+    out = tq2.gemm(x, W)
+    assert np.array_equal(out, np.zeros((M, N)))
+
+
+def test_all_codes_two_closed_form():
+    # out[m,n] = sum_blk d[n,blk] * sum_{k in blk} x[m,k]
+    N, K, M = 7, 512, 4
+    nb = K // 128
+    codes = np.full((N, K), 2, dtype=np.uint8)
+    d_bits = synth.f16_bits(synth.uniform(N * nb, 2, 0.01, 0.1)).reshape(N, nb)
+    d = d_bits.view(np.float16).astype(np.float64)
+    x = synth.random_x(M, K, 4).astype(np.float64)
+    out = tq2.gemm(x, tq2.dequant_aos(synth.pack_aos(codes, d_bits), N, K))
+    blocksum = x.reshape(M, nb, 128).sum(axis=2)           # [M][nb]
+    want = np.array([[sum(d[n, b] * blocksum[m, b] for b in range(nb)) for n in range(N)]
+                     for m in range(M)])
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_unit_vectors_recover_columns():
+    # N != K so a transposed operand cannot even run; e_k picks column k of W
+    N, K = 3, 256
+    aos = synth.random_tq2(N, K, 20)
+    codes, d_bits = tq2.parse_aos(aos, N, K)
+    d = d_bits.view(np.float16).astype(np.float64)
+    for k in (0, 1, 5, 127, 128, 200, 255):
+        x = np.zeros((1, K))
+        x[0, k] = 1.0
+        out = tq2.gemm(x, tq2.dequant(codes, d_bits))
+        want = (codes[:, k].astype(np.float64) - 1.0) * d[:, k // 128]
+        assert np.array_equal(out[0], want)
+
+
+def test_linearity():
+    N, K = 9, 384
+    W = tq2.dequant_aos(synth.random_tq2(N, K, 30), N, K)
+    x1 = synth.random_x(3, K, 31).astype(np.float64)
+    x2 = synth.random_x(3, K, 32).astype(np.float64)
+    a, b = 0.75, -1.5
+    np.testing.assert_allclose(tq2.gemm(a * x1 + b * x2, W),
+                               a * tq2.gemm(x1, W) + b * tq2.gemm(x2, W), rtol=1e-12, atol=1e-12)
+
+
+def test_dequant_f16_is_exact():
+    N, K = 6, 256
+    aos = synth.random_tq2(N, K, 40)
+    codes, d_bits = tq2.parse_aos(aos, N, K)
+    bits = tq2.dequant_f16_bits(codes, d_bits)
+    back = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(back, tq2.dequant(codes, d_bits))
+    assert set(np.unique(codes)) <= {0, 1, 2}
+
+
+def test_page_cpu_reference_loop_on_page_data():
+    # the page's own reference: dequant to f32, then a naive f32 loop
+    aos, N, K, xs = synth.tiny_tq2(M_list=(1, 7, 8, 9))
+    W = tq2.dequant_aos(aos, N, K)
+    W32 = W.astype(np.float32)
+    for M, x in list(xs.items()) + [(3, synth.page_x(3, K))]:
+        ref = np.zeros((M, N), dtype=np.float32)
+        for m in range(M):
+            for n in range(N):
+                acc = np.float32(0.0)
+                for k in range(K):
+                    acc = np.float32(acc + x[m, k] * W32[n, k])
+                ref[m, n] = acc
+        out = tq2.gemm(x, W)
+        assert np.max(np.abs(out - ref)) < 1e-4
+        assert np.any(np.abs(out) > 1e-6)
+
+
+def test_gemm_elem_matches_full():
+    N, K, M = 11, 640, 2
+    aos = synth.random_tq2(N, K, 50)
+    codes, d_bits = tq2.parse_aos(aos, N, K)
+    x = synth.random_x(M, K, 51)
+    W = tq2.dequant(codes, d_bits)
+    full, fa = tq2.gemm(x, W), tq2.gemm_abs(x, W)
+    for m in range(M):
+        for n in range(N):
+            v, a = tq2.gemm_elem(x[m], codes[n], d_bits[n])
+            assert abs(v - full[m, n]) < 1e-12 and abs(a - fa[m, n]) < 1e-12
+
+
+def test_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        tq2.parse_aos(b"\0" * 34, 1, 100)
+    with pytest.raises(ValueError):
+        tq2.parse_aos(b"\0" * 33, 1, 128)
