@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed ternary GEMM (and the rest of the hot path).
+
+Headline workload: the TQ2 GEMV (decode shape) M=1, N=K=4096, codes iid
+uniform over {0,1,2}, per-block f16 scales iid U(0.01, 0.1), x iid N(0,1).
+One *step* is one CUDA-graph replay of 64 GEMVs, each against its own copy
+of the weight (64 x 4.46 MB = 285 MB > the 129 MB L2, so every GEMV streams
+its weight from HBM).  ``value`` is packed-weight GB/s over the whole job:
+(N*K/4 + N*K/128*2) bytes per GEMV x GEMVs / device time.
+
+The same JSON line carries, under ``extra``, the other workloads of the hot
+path measured the same way (skinny M=8/32/128 x N=11008, large M=4096 x
+N=14336, and the blr layer once built), each with its roofline fraction.
+
+``--impl reference`` times the f64 CPU oracle instead (a deliberately slow
+reference on the host cores; see ``oracle/``).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+GEMV_COPIES = 64
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    p.add_argument("--only", default="", help="comma list of extra workloads to run")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "binary_packed_weight_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels
+    have not changed since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(key)
+    if not d or d.get("src_hash") != src_hash():
+        return None
+    return d.get("dram_bytes")
+
+
+# ---------------------------------------------------------------- clocks ----
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons around a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        busy = sorted(sm)[len(sm) // 4:] if sm else []
+        return {"sm_mhz": float(np.median(busy)) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- timing ----
+def time_graph(torch, fn, steps, warmup, stream):
+    """Capture fn() once into a CUDA graph; replay warmup + steps times; return
+    device seconds of the timed replays (CUDA events on the launch stream)."""
+    with torch.cuda.stream(stream):
+        fn()                                   # first call outside capture (allocator pools)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3, g
+
+
+def gemv_bytes(N, K):
+    return N * K // 4 + N * (K // 128) * 2
+
+
+# ------------------------------------------------------------- workloads ----
+def run_gemv(torch, bpw, args, stream, dev):
+    cfg = synth.GEMV
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    aos = synth.random_tq2(N, K, cfg["wkey"])
+    ws = [bpw.tq2_upload(aos, N, K) for _ in range(GEMV_COPIES)]
+    x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
+    out = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    def step():
+        for w in ws:
+            bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
+
+    clocks = Clocks(dev.index if dev.index is not None else 0)
+    # capture + warm up, then the clocked, timed region
+    secs, g = None, None
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    return dict(ws=ws, x=x, out=out, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
+
+
+def e2e_gemv(torch, bpw, ctx, stream, reps):
+    """Public API with host buffers: pinned x -> device, tq2_gemm, out -> pinned host."""
+    M, N, K = ctx["M"], ctx["N"], ctx["K"]
+    xh = torch.from_numpy(synth.random_x(M, K, synth.GEMV["xkey"])).pin_memory()
+    oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    xd, od = ctx["x"], ctx["out"]
+    for _ in range(3):
+        for w in ctx["ws"]:
+            with torch.cuda.stream(stream):
+                xd.copy_(xh, non_blocking=True)
+                bpw.tq2_gemm(w, xd, od, stream=stream.cuda_stream)
+                oh.copy_(od, non_blocking=True)
+    stream.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for w in ctx["ws"]:
+            with torch.cuda.stream(stream):
+                xd.copy_(xh, non_blocking=True)
+                bpw.tq2_gemm(w, xd, od, stream=stream.cuda_stream)
+                oh.copy_(od, non_blocking=True)
+        stream.synchronize()
+    dt = time.perf_counter() - t0
+    n = reps * len(ctx["ws"])
+    return dict(value=gemv_bytes(N, K) * n / dt / 1e9, unit="GB/s",
+                h2d_bytes_per_step=M * K * 4 * len(ctx["ws"]), d2h_bytes_per_step=M * N * 4 * len(ctx["ws"]))
+
+
+def extra_skinny(torch, bpw, stream, dev, pk, Ms):
+    cfg = synth.SKINNY
+    N, K = cfg["N"], cfg["K"]
+    aos = synth.random_tq2(N, K, cfg["wkey"])
+    copies = 24                                            # 24 x 12 MB > L2
+    ws = [bpw.tq2_upload(aos, N, K) for _ in range(copies)]
+    res = {}
+    for M in Ms:
+        x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def step():
+            for w in ws:
+                bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
+        secs, _ = time_graph(torch, step, 20, 3, stream)
+        t = secs / (20 * copies)
+        wb = gemv_bytes(N, K)
+        alg = wb + M * K * 4 + M * N * 4
+        flops = 2.0 * M * N * K
+        tfl = flops / t / 1e12
+        bound = "hbm" if M <= 32 else "tensor"
+        res[f"M{M}"] = dict(us=t * 1e6, tflops=tfl, weight_gbs=wb / t / 1e9, alg_gbs=alg / t / 1e9,
+                            hbm_frac=alg / t / 1e9 / pk["hbm"], tensor_frac=tfl / pk["bf16"],
+                            bound=bound, path="skinny" if M <= 16 else "tensor")
+    for w in ws:
+        w.free()
+    return res
+
+
+def extra_large(torch, bpw, stream, dev, pk):
+    cfg = synth.LARGE
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    aos = synth.random_tq2(N, K, cfg["wkey"])
+    w = bpw.tq2_upload(aos, N, K)
+    x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
+    out = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    def step():
+        bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
+    secs, _ = time_graph(torch, step, 10, 3, stream)
+    t = secs / 10
+    flops = 2.0 * M * N * K
+    tfl = flops / t / 1e12
+    w.free()
+    return dict(us=t * 1e6, tflops=tfl, weight_gbs=gemv_bytes(N, K) / t / 1e9, tensor_frac=tfl / pk["bf16"],
+                tensor_frac_sustained=tfl / pk["bf16_sus"] if pk.get("bf16_sus") else None,
+                bound="tensor", includes="x f32->f16 staging kernel + GEMM")
+
+
+# ------------------------------------------------------------ cpu oracle ----
+def oracle_gemv_sample(budget_s=12.0):
+    """The f64 oracle on the GEMV workload, repeated for about budget_s seconds."""
+    from oracle import tq2 as otq2
+    cfg = synth.GEMV
+    N, K = cfg["N"], cfg["K"]
+    aos = synth.random_tq2(N, K, cfg["wkey"])
+    x = synth.random_x(1, K, cfg["xkey"])
+    n = 0
+    c0, t0 = os.times(), time.perf_counter()
+    while True:
+        W = otq2.dequant_aos(aos, N, K)
+        otq2.gemm(x, W)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    c1 = os.times()
+    cpu = (c1.user - c0.user) + (c1.system - c0.system)
+    return dict(value=gemv_bytes(N, K) * n / dt / 1e9, unit="GB/s", cores=max(1, round(cpu / dt)),
+                kind="oracle", sample=f"{n} full GEMVs M=1 N=K=4096 (AoS parse + f64 dequant + f64 GEMV) "
+                                      f"in {dt:.1f} s; cpu/wall {cpu / dt:.2f}")
+
+
+# ------------------------------------------------------------------ main ----
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg_name = "tq2_gemv M=1 N=4096 K=4096"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = oracle_gemv_sample(budget_s=max(3.0, min(60.0, 0.5 * (args.steps + args.warmup))))
+        line = dict(metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
+                    value=cb["value"], unit="GB/s", impl="reference", n_gpus=args.gpus, steps=args.steps,
+                    warmup=args.warmup, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                    data="synthetic", config={"workload": cfg_name, "weights": "packed BlockTQ2_0_g128"},
+                    cpu_baseline=cb, e2e={"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0})
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import binary_packed_weight_gb300 as bpw
+    from binary_packed_weight_gb300 import build as _b
+    _b.build()
+    bpw.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    ctx = run_gemv(torch, bpw, args, stream, dev)
+    g, clocks = ctx["graph"], ctx["clocks"]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    secs = e0.elapsed_time(e1) / 1e3
+    if dist:
+        t = torch.tensor([secs], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+        dist.barrier()
+    N, K, M = ctx["N"], ctx["K"], ctx["M"]
+    gemvs = args.steps * GEMV_COPIES
+    wbytes = gemv_bytes(N, K)
+    value = wbytes * gemvs * world / secs / 1e9
+    t_launch = secs / gemvs
+    alg = wbytes + M * K * 4 + M * N * 4
+    achieved = alg / t_launch / 1e9
+    e2e = e2e_gemv(torch, bpw, ctx, stream, reps=max(2, min(20, args.steps // 50)))
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        only = set(filter(None, args.only.split(",")))
+        if not only or "skinny" in only:
+            extra["tq2_skinny_N11008"] = extra_skinny(torch, bpw, stream, dev, pk, (8, 32, 128))
+        if not only or "large" in only:
+            extra["tq2_large_M4096_N14336"] = extra_large(torch, bpw, stream, dev, pk)
+
+    if rank != 0:
+        return
+    cb = oracle_gemv_sample(budget_s=12.0) if world == 1 else None
+    line = dict(
+        metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
+        value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=secs / args.steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="f32", data="synthetic",
+        config={"workload": cfg_name, "gemvs_per_step": GEMV_COPIES,
+                "l2": f"inputs larger than L2: {GEMV_COPIES} distinct weight copies "
+                      f"({GEMV_COPIES * wbytes / 1e6:.0f} MB) rotated every step",
+                "weights": "packed BlockTQ2_0_g128, 2 bits + f16 scale per 128",
+                "activations": "f32 (split to two f16 terms on the GPU), f32 accumulation",
+                "value": "packed-weight bytes per GEMV x GEMVs / device seconds",
+                "parallelism": "replicas" if world > 1 else "single GPU"},
+        tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
+        roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                  "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv"),
+                  "kernel": "stage_x_frag + tq2_skinny (per GEMV, average over the timed graph replays)",
+                  "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"] + " hbm_gbs (copy)"},
+        cpu_baseline=cb, e2e=e2e, gpu_launches=2 * gemvs, clocks=clk, extra=extra,
+    )
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+"""Python binding of the tq2-gb300 C ABI (``include/tq2.h``).
+
+Argument marshalling only: every function forwards device pointers, sizes
+and the current CUDA stream of torch to the shared library
+``libtq2gb300.so`` built from ``csrc/``.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+
+Tensors must live on the current CUDA device, be contiguous and have the
+dtype the C ABI states (float32 for activations and outputs, uint8 / int16
+bit patterns for packed data).
+"""
+import ctypes
+import os
+
+__all__ = [
+    "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
+    "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
+    "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
+]
+
+PATH_AUTO, PATH_SKINNY, PATH_TENSOR = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libtq2gb300.so")
+_lib = None
+
+_P, _I64, _I, _F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_SIGS = {
+    "tq2_status_string": (ctypes.c_char_p, [_I]),
+    "tq2_last_error": (ctypes.c_char_p, []),
+    "tq2_version": (ctypes.c_char_p, []),
+    "tq2_device_status": (_I, [_P]),
+    "tq2_upload": (_I, [_P, _I64, _I64, ctypes.POINTER(_P), _P]),
+    "tq2_free": (_I, [_P]),
+    "tq2_shape": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "tq2_gemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "tq2_gemm_path": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "tq2_unpack": (_I, [_P, _P, _P]),
+    "tq2_dequant_f16": (_I, [_P, _P, _P]),
+    "blr_expand_bits": (_I, [_P, _I64, _I64, _P, _I, _P]),
+    "blr_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "blr_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                          _I64, _I64, _I64, _I64, _F, _P]),
+}
+
+
+class TQ2Error(RuntimeError):
+    def __init__(self, status, where):
+        msg = load().tq2_last_error().decode(errors="replace")
+        name = load().tq2_status_string(status).decode()
+        super().__init__(f"{where}: {name} ({status}): {msg}")
+        self.status = status
+
+
+def load():
+    """Load the shared library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is missing; build it with binary_packed_weight_gb300.build.build()")
+        lib = ctypes.CDLL(lib_path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _check(status, where):
+    if status != 0:
+        raise TQ2Error(status, where)
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Weight:
+    """A ``BlockTQ2_0_g128`` weight resident on the GPU (owns a C handle)."""
+
+    def __init__(self, handle, N, K):
+        self._h, self.N, self.K = handle, N, K
+
+    @property
+    def handle(self):
+        return self._h
+
+    def free(self):
+        if self._h:
+            _check(load().tq2_free(self._h), "tq2_free")
+            self._h = None
+
+    def __del__(self):
+        try:
+            if self._h and _lib is not None:
+                _lib.tq2_free(self._h)
+        except Exception:
+            pass
+
+
+def tq2_upload(aos, N, K, stream=None):
+    """Upload AoS block bytes (host ``bytes`` / numpy uint8) -> :class:`Weight`."""
+    buf = bytes(aos) if not isinstance(aos, (bytes, bytearray)) else aos
+    arr = (ctypes.c_uint8 * len(buf)).from_buffer_copy(buf)
+    h = ctypes.c_void_p()
+    _check(load().tq2_upload(ctypes.cast(arr, _P), N, K, ctypes.byref(h), _stream(stream)), "tq2_upload")
+    return Weight(h.value, N, K)
+
+
+def tq2_gemm(w, x, out, stream=None):
+    M, K = x.shape
+    _check(load().tq2_gemm(w.handle, _ptr(x), _ptr(out), M, w.N, K, _stream(stream)), "tq2_gemm")
+    return out
+
+
+def tq2_gemm_path(w, x, out, path, stream=None):
+    M, K = x.shape
+    _check(load().tq2_gemm_path(w.handle, _ptr(x), _ptr(out), M, w.N, K, path, _stream(stream)), "tq2_gemm_path")
+    return out
+
+
+def tq2_unpack(w, stream=None):
+    n = w.N * (w.K // 128) * 34
+    buf = (ctypes.c_uint8 * n)()
+    _check(load().tq2_unpack(w.handle, ctypes.cast(buf, _P), _stream(stream)), "tq2_unpack")
+    return bytes(buf)
+
+
+def tq2_dequant_f16(w, out_u16, stream=None):
+    _check(load().tq2_dequant_f16(w.handle, _ptr(out_u16), _stream(stream)), "tq2_dequant_f16")
+    return out_u16
+
+
+def blr_expand_bits(bits, rows, r, plane, transpose, stream=None):
+    _check(load().blr_expand_bits(_ptr(bits), rows, r, _ptr(plane), int(transpose), _stream(stream)),
+           "blr_expand_bits")
+    return plane
+
+
+def blr_forward(bits_u, bits_v, h, l, g, x, y, a_save, c_save=None, stream=None):
+    T, d_in = x.shape
+    d_out, r = h.numel(), l.numel()
+    _check(load().blr_forward(_ptr(bits_u), _ptr(bits_v), _ptr(h), _ptr(l), _ptr(g), _ptr(x), _ptr(y),
+                              _ptr(a_save), _ptr(c_save), T, d_in, d_out, r, _stream(stream)), "blr_forward")
+    return y
+
+
+def blr_backward(bits_u, bits_v, h, l, g, x, dy, a_save, c_save, dx, dh, dl, dg, gscale=1.0, stream=None):
+    T, d_in = x.shape
+    d_out, r = h.numel(), l.numel()
+    _check(load().blr_backward(_ptr(bits_u), _ptr(bits_v), _ptr(h), _ptr(l), _ptr(g), _ptr(x), _ptr(dy),
+                               _ptr(a_save), _ptr(c_save), _ptr(dx), _ptr(dh), _ptr(dl), _ptr(dg),
+                               T, d_in, d_out, r, float(gscale), _stream(stream)), "blr_backward")
+    return dx
+
+
+def device_status(stream=None):
+    """Synchronize and raise if a kernel recorded a bounded-wait timeout."""
+    _check(load().tq2_device_status(_stream(stream)), "tq2_device_status")

@@ -1,0 +1,71 @@
+// tq2_internal.h -- declarations shared by the library's translation units
+// (host side only).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+struct tq2_weight {
+    int64_t N = 0, K = 0;
+    uint8_t* codes = nullptr;      // [N][K/4]
+    uint16_t* scales = nullptr;    // [N][K/128] f16 bits
+    int device = 0;
+    CUtensorMap codes_map;         // 2D map over the code plane (bytes), built at upload
+    bool has_codes_map = false;
+};
+
+namespace tq2 {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream drains; it must call griddepcontrol.wait
+// before touching anything that earlier work writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// tq2_skinny.cu
+cudaError_t launch_repack(const uint8_t* aos_dev, uint8_t* codes, uint16_t* scales, int64_t nblocks,
+                          cudaStream_t st);
+cudaError_t launch_unpack(const uint8_t* codes, const uint16_t* scales, uint8_t* aos_dev, int64_t nblocks,
+                          cudaStream_t st);
+cudaError_t launch_dequant_f16(const uint8_t* codes, const uint16_t* scales, uint16_t* w, int64_t N,
+                               int64_t K, cudaStream_t st);
+size_t skinny_scratch_bytes(int64_t M, int64_t K);
+cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M,
+                          int N, int K, void* scratch, cudaStream_t st);
+unsigned int read_clear_dev_error_skinny(cudaStream_t st);
+
+// tq2_umma.cu
+size_t tensor_scratch_bytes(int64_t M, int64_t K);
+cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
+                          cudaStream_t st);
+unsigned int read_clear_dev_error_umma(cudaStream_t st);
+
+// blr.cu
+cudaError_t launch_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, uint16_t* plane, int transpose,
+                               cudaStream_t st);
+unsigned int read_clear_dev_error_blr(cudaStream_t st);
+
+// api.cu: record the calling thread's last error message; returns `st`.
+int set_error(int st, const char* fmt, ...);
+
+// tensor maps (api.cu): 2D tiled map, inner dimension first.
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle swizzle);
+
+}  // namespace tq2

@@ -1,0 +1,294 @@
+// tq2_skinny.cu -- weight repack / unpack / dequant kernels and the skinny
+// (M <= 16) ternary GEMM.
+//
+// Format: BlockTQ2_0_g128 ("oxibonsai-kernels 0.2.1, src/gpu_backend/
+// metal_graph/tests_gemm_tq2.rs", test test_encode_gemm_tq2_matches_reference):
+// per 128-wide block of a weight row, 32 bytes of 2-bit codes (element 4j+i at
+// bits 2i of byte j) and an f16 scale d; W[n,k] = (c-1)*d.
+//
+// Device layout ("SoA"): codes uint8[N][K/4] (each row's qs bytes in K order),
+// scales uint16[N][K/128] (f16 bits).
+//
+// Skinny GEMM: out[m,n] = sum_k x[m,k] W[n,k] for M <= 16 with f32
+// activations.  The contraction runs on mma.sync m16n8k16 (f16 in, f32
+// accumulate) because at M <= 16 the kernel is bound by issue slots: one
+// HMMA replaces 2*M FFMAs per weight per thread.  Each x is split exactly
+// enough into hi = f16(x) and lo = f16(x - hi) (two B columns), which leaves
+// a relative residual below 2^-21.  Weights enter the MMA as (c-1) in f16
+// (exact); the block scale d multiplies the f32 block partial afterwards.
+#include "ptx.cuh"
+#include "tq2_internal.h"
+
+namespace tq2 {
+
+// --------------------------------------------------------------------------
+// repack AoS (34-byte blocks) -> SoA planes, and back
+// --------------------------------------------------------------------------
+__global__ void repack_aos_kernel(const uint8_t* __restrict__ aos, uint8_t* __restrict__ codes,
+                                  uint16_t* __restrict__ scales, int64_t nblocks) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;  // one byte of qs
+    if (i >= nblocks * 32) return;
+    const int64_t b = i >> 5;
+    const int j = (int)(i & 31);
+    const uint8_t* blk = aos + b * 34;
+    codes[b * 32 + j] = blk[j];
+    if (j == 0) scales[b] = (uint16_t)(blk[32] | ((uint16_t)blk[33] << 8));
+}
+
+__global__ void unpack_soa_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                                  uint8_t* __restrict__ aos, int64_t nblocks) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= nblocks * 32) return;
+    const int64_t b = i >> 5;
+    const int j = (int)(i & 31);
+    uint8_t* blk = aos + b * 34;
+    blk[j] = codes[b * 32 + j];
+    if (j == 0) {
+        const uint16_t d = scales[b];
+        blk[32] = (uint8_t)(d & 0xFF);
+        blk[33] = (uint8_t)(d >> 8);
+    }
+}
+
+// W as f16 bits, natural order, through the same pair decode the GEMMs use:
+// one thread per 32-bit code word (16 elements).
+__global__ void dequant_f16_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                                   uint16_t* __restrict__ w, int64_t N, int64_t K) {
+    const int64_t wi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int64_t words_per_row = K / 16;
+    if (wi >= N * words_per_row) return;
+    const int64_t n = wi / words_per_row;
+    const int64_t k0 = (wi % words_per_row) * 16;
+    const uint32_t word = reinterpret_cast<const uint32_t*>(codes)[wi];
+    const uint16_t dbits = scales[n * (K / 128) + k0 / 128];
+    const __half2 d2 = __halves2half2(__ushort_as_half(dbits), __ushort_as_half(dbits));
+    uint32_t p[8];
+    decode_word(word, p);
+    uint16_t* dst = w + n * K + k0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        __half2 v = __hmul2(*reinterpret_cast<__half2*>(&p[q]), d2);
+        dst[q] = __half_as_ushort(__low2half(v));
+        dst[q + 8] = __half_as_ushort(__high2half(v));
+    }
+}
+
+// --------------------------------------------------------------------------
+// skinny GEMM
+// --------------------------------------------------------------------------
+// Staged B fragments.  For n8 tile j, k16 step ks = 8*kb + s (kb: 128-block,
+// s: step within the block) and lane (gq = lane/4, tq = lane%4) the uint2
+// holds the two B registers of mma.m16n8k16: column gq is token 4j + gq/2,
+// part gq%2 (0: hi, 1: lo); the K slots map to the A decode order:
+//   b0,b1 = x[kbase + q], x[kbase + q + 8];  b2,b3 = x[kbase + q + 1], x[kbase + q + 9]
+// with kbase = 128*kb + 32*tq + 16*(s/4) and q = 2*(s%4).
+__device__ __forceinline__ uint16_t split_part(float v, int part) {
+    const __half hi = __float2half_rn(v);
+    if (part == 0) return __half_as_ushort(hi);
+    return __half_as_ushort(__float2half_rn(v - __half2float(hi)));
+}
+
+__global__ void stage_x_frag_kernel(const float* __restrict__ x, uint2* __restrict__ xs, int M, int K,
+                                    int ntiles) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int KS = K >> 4;
+    const int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)ntiles * KS * 32) return;
+    const int lane = (int)(idx & 31);
+    const int64_t rest = idx >> 5;
+    const int ks = (int)(rest % KS);
+    const int j = (int)(rest / KS);
+    const int col = 8 * j + (lane >> 2);
+    const int m = col >> 1, part = col & 1;
+    if (m >= M) {
+        xs[idx] = make_uint2(0u, 0u);
+        return;
+    }
+    const int kb = ks >> 3, s = ks & 7;
+    const int k = kb * 128 + 32 * (lane & 3) + 16 * (s >> 2) + 2 * (s & 3);
+    const float* xr = x + (int64_t)m * K + k;
+    const uint32_t b01 = (uint32_t)split_part(xr[0], part) | ((uint32_t)split_part(xr[8], part) << 16);
+    const uint32_t b23 = (uint32_t)split_part(xr[1], part) | ((uint32_t)split_part(xr[9], part) << 16);
+    xs[idx] = make_uint2(b01, b23);
+}
+
+// Pair q of a code word, q in 0..7 (elements q and q+8 of the word).
+template <int Q>
+__device__ __forceinline__ uint32_t pair_q(uint32_t w) {
+    if constexpr (Q < 4) return decode_pair<2 * Q>(w);
+    else return decode_pair<2 * (Q - 4)>(w >> 8);
+}
+
+__device__ __forceinline__ uint2 ldg_u2(const uint8_t* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// One CTA owns 16 weight rows (one m16 fragment); its W warps split the
+// K blocks and reduce through shared memory.  Lane (g, t) of a warp reads
+// bytes 8t..8t+7 of the 32-byte block of rows g and g+8: two code words per
+// row per block, i.e. the 4 k16 steps s = 4*word + 0..3 of that word.
+template <int NT>
+__global__ void __launch_bounds__(256) tq2_skinny_kernel(const uint8_t* __restrict__ codes,
+                                                         const uint16_t* __restrict__ scales,
+                                                         const uint2* __restrict__ xs,
+                                                         float* __restrict__ out, int M, int N, int K) {
+    constexpr int CH = 4;                      // blocks loaded ahead per warp
+    __shared__ float red[8][16][17];           // [warp][token][row]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int n0 = blockIdx.x * 16;
+    const int nb = K >> 7;
+    const int KS = K >> 4;
+    const int kb_begin = (nb * warp) / W, kb_end = (nb * (warp + 1)) / W;
+    const int rowA = n0 + g, rowB = n0 + g + 8;
+    const bool okA = rowA < N, okB = rowB < N;
+    const int64_t pitch = K >> 2;
+    const uint8_t* pA = codes + (int64_t)(okA ? rowA : 0) * pitch + 8 * t;
+    const uint8_t* pB = codes + (int64_t)(okB ? rowB : 0) * pitch + 8 * t;
+    const uint16_t* sA = scales + (int64_t)(okA ? rowA : 0) * nb;
+    const uint16_t* sB = scales + (int64_t)(okB ? rowB : 0) * nb;
+
+    pdl_launch_dependents();
+
+    float tot[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[j][i] = 0.f;
+
+    bool waited = false;
+#pragma unroll 1
+    for (int kb0 = kb_begin; kb0 < kb_end; kb0 += CH) {
+        uint2 cA[CH], cB[CH];
+        float dA[CH], dB[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int kb = kb0 + c;
+            const bool v = kb < kb_end;
+            cA[c] = (v && okA) ? ldg_u2(pA + kb * 32) : make_uint2(0u, 0u);
+            cB[c] = (v && okB) ? ldg_u2(pB + kb * 32) : make_uint2(0u, 0u);
+            dA[c] = (v && okA) ? __half2float(__ushort_as_half(__ldg(sA + kb))) : 0.f;
+            dB[c] = (v && okB) ? __half2float(__ushort_as_half(__ldg(sB + kb))) : 0.f;
+        }
+        if (!waited) {           // the weights are immutable; x may come from the previous kernel
+            pdl_wait();
+            waited = true;
+        }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int kb = kb0 + c;
+            if (kb >= kb_end) break;
+            float acc[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+            const uint2* xb = xs + ((int64_t)kb * 8) * 32 + lane;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t wa = (s < 4) ? cA[c].x : cA[c].y;
+                const uint32_t wb = (s < 4) ? cB[c].x : cB[c].y;
+                uint32_t a[4];
+                switch (s & 3) {
+                    case 0: a[0] = pair_q<0>(wa); a[1] = pair_q<0>(wb); a[2] = pair_q<1>(wa); a[3] = pair_q<1>(wb); break;
+                    case 1: a[0] = pair_q<2>(wa); a[1] = pair_q<2>(wb); a[2] = pair_q<3>(wa); a[3] = pair_q<3>(wb); break;
+                    case 2: a[0] = pair_q<4>(wa); a[1] = pair_q<4>(wb); a[2] = pair_q<5>(wa); a[3] = pair_q<5>(wb); break;
+                    default: a[0] = pair_q<6>(wa); a[1] = pair_q<6>(wb); a[2] = pair_q<7>(wa); a[3] = pair_q<7>(wb); break;
+                }
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const uint2 b = xb[((int64_t)j * KS + s) * 32];
+                    mma_16816(acc[j], a, b.x, b.y, acc[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                tot[j][0] = fmaf(dA[c], acc[j][0], tot[j][0]);
+                tot[j][1] = fmaf(dA[c], acc[j][1], tot[j][1]);
+                tot[j][2] = fmaf(dB[c], acc[j][2], tot[j][2]);
+                tot[j][3] = fmaf(dB[c], acc[j][3], tot[j][3]);
+            }
+        }
+    }
+    if (!waited) pdl_wait();
+
+    // Columns 2t, 2t+1 of tile j are token 4j+t (hi, lo).
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int m = 4 * j + t;
+        red[warp][m][g] = tot[j][0] + tot[j][1];
+        red[warp][m][g + 8] = tot[j][2] + tot[j][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < M * 16; i += blockDim.x) {
+        const int m = i >> 4, r = i & 15;
+        float s = 0.f;
+        for (int w = 0; w < W; ++w) s += red[w][m][r];
+        if (n0 + r < N) out[(int64_t)m * N + n0 + r] = s;
+    }
+}
+
+// --------------------------------------------------------------------------
+// host launchers
+// --------------------------------------------------------------------------
+cudaError_t launch_repack(const uint8_t* aos_dev, uint8_t* codes, uint16_t* scales, int64_t nblocks,
+                          cudaStream_t st) {
+    const int64_t n = nblocks * 32;
+    repack_aos_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(aos_dev, codes, scales, nblocks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint8_t* codes, const uint16_t* scales, uint8_t* aos_dev, int64_t nblocks,
+                          cudaStream_t st) {
+    const int64_t n = nblocks * 32;
+    unpack_soa_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(codes, scales, aos_dev, nblocks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_f16(const uint8_t* codes, const uint16_t* scales, uint16_t* w, int64_t N, int64_t K,
+                               cudaStream_t st) {
+    const int64_t n = N * (K / 16);
+    dequant_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(codes, scales, w, N, K);
+    return cudaGetLastError();
+}
+
+size_t skinny_scratch_bytes(int64_t M, int64_t K) {
+    const int64_t ntiles = (M + 3) / 4;
+    return (size_t)(ntiles * (K / 16) * 32) * sizeof(uint2);
+}
+
+cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M,
+                          int N, int K, void* scratch, cudaStream_t st) {
+    const int ntiles = (M + 3) / 4;
+    uint2* xs = reinterpret_cast<uint2*>(scratch);
+    const int64_t nthr = (int64_t)ntiles * (K / 16) * 32;
+    cudaError_t e = launch_pdl(stage_x_frag_kernel, dim3((unsigned)((nthr + 255) / 256)), dim3(256), 0, st,
+                               x, xs, M, K, ntiles);
+    if (e != cudaSuccess) return e;
+    const int nb = K / 128;
+    const int W = nb < 8 ? nb : 8;
+    const dim3 grid((unsigned)((N + 15) / 16)), block((unsigned)(32 * W));
+    const uint2* cxs = xs;
+    switch (ntiles) {
+        case 1: return launch_pdl(tq2_skinny_kernel<1>, grid, block, 0, st, codes, scales, cxs, out, M, N, K);
+        case 2: return launch_pdl(tq2_skinny_kernel<2>, grid, block, 0, st, codes, scales, cxs, out, M, N, K);
+        case 3: return launch_pdl(tq2_skinny_kernel<3>, grid, block, 0, st, codes, scales, cxs, out, M, N, K);
+        case 4: return launch_pdl(tq2_skinny_kernel<4>, grid, block, 0, st, codes, scales, cxs, out, M, N, K);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+unsigned int read_clear_dev_error_skinny(cudaStream_t st) {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_dev_error, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return 0;
+    cudaMemcpyToSymbolAsync(g_dev_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+    cudaStreamSynchronize(st);
+    return v;
+}
+
+}  // namespace tq2

@@ -1,0 +1,231 @@
+/*
+ * tq2.h -- C ABI of the packed low-bit weight GEMM library for GB300 (sm_103a).
+ *
+ * One operation sits under two consumers:
+ *
+ *     out[m,n] = sum_k x[m,k] * W[n,k]
+ *
+ *  1. W in the ternary block format BlockTQ2_0_g128
+ *     ("oxibonsai-kernels 0.2.1, src/gpu_backend/metal_graph/tests_gemm_tq2.rs",
+ *     test test_encode_gemm_tq2_matches_reference): each 128-wide block of a
+ *     weight row holds 32 bytes of 2-bit codes, 4 per byte, least significant
+ *     first, code c meaning c-1 in {-1,0,+1}, and one f16 scale d;
+ *     W[n,k] = (c-1)*d.
+ *  2. The binary low-rank layer blr
+ *     ("cortiq-engine 0.8.43, src/gpu_wgpu/train_mm.rs", module doc,
+ *     blr_forward, blr_backward): W = diag(h) S_U diag(l) S_V^T diag(g) with
+ *     the +-1 factors S_U, S_V stored as 1-bit bitmaps.
+ *
+ * Conventions for every entry point
+ *   - Every call returns a tq2_status; nothing aborts the process.  Argument
+ *     and shape errors are detected on the host before anything is launched.
+ *     tq2_last_error() gives a one-line message for the calling thread.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Compute calls are asynchronous on that stream unless stated.
+ *   - "DEVICE" pointers are CUDA device memory owned by the caller (for
+ *     instance torch tensors); "HOST" pointers are ordinary host memory.
+ *   - All float data is IEEE binary32, row-major, densely packed.
+ *   - Device-side waits inside the kernels are bounded (about one second);
+ *     when one runs out the kernel records TQ2_ETIMEOUT and returns early.
+ *     tq2_device_status() reports (and clears) that record.
+ *   - Activations are staged to f16 on the GPU; entries must be finite with
+ *     |v| < 65504 or the results are not finite.
+ */
+#ifndef TQ2_GB300_H
+#define TQ2_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TQ2_API __attribute__((visibility("default")))
+#else
+#define TQ2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ2_OK = 0,
+    TQ2_EINVAL = 1,          /* null pointer or bad argument value            */
+    TQ2_ESHAPE = 2,          /* sizes break a documented shape rule           */
+    TQ2_ENOMEM = 3,          /* device or host allocation failed              */
+    TQ2_ECUDA = 4,           /* a CUDA runtime/driver call failed             */
+    TQ2_ETIMEOUT = 5,        /* a bounded device-side wait ran out            */
+    TQ2_EUNSUPPORTED = 6     /* no kernel for this device or configuration    */
+} tq2_status;
+
+/* Opaque weight handle; the library owns the device planes behind it. */
+typedef struct tq2_weight* tq2_handle;
+
+/* Kernel selection for tq2_gemm_path (tests and benchmarks). */
+typedef enum {
+    TQ2_PATH_AUTO = 0,       /* M <= 16: skinny kernel; otherwise tensor path */
+    TQ2_PATH_SKINNY = 1,     /* decode-in-register kernel, f32 activations, M <= 16 */
+    TQ2_PATH_TENSOR = 2      /* tcgen05 kernel, activations staged to f16     */
+} tq2_path;
+
+/* Static string for a status code. */
+TQ2_API const char* tq2_status_string(int status);
+
+/* Message of the last failure on the calling thread ("" if none). */
+TQ2_API const char* tq2_last_error(void);
+
+/* Library build identification, e.g. "tq2-gb300 sm_103a". */
+TQ2_API const char* tq2_version(void);
+
+/*
+ * Synchronize `stream`, then report and clear the device-side error record
+ * (TQ2_ETIMEOUT if a bounded wait in any kernel ran out since the last call,
+ * TQ2_ECUDA if the stream reports an error, else TQ2_OK).
+ */
+TQ2_API tq2_status tq2_device_status(void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Ternary TQ2 weights                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tq2_upload -- copy BlockTQ2_0_g128 blocks to the device and repack them.
+ * Passage: the public SoA cache path get_or_upload_tq2_weight_soa(key, aos)
+ * of test test_encode_gemm_tq2_matches_reference ("oxibonsai-kernels 0.2.1,
+ * tests_gemm_tq2.rs").
+ *
+ *   aos     HOST, N*(K/128) blocks of 34 bytes, row-major (block kb of row n
+ *           at index n*(K/128)+kb).  Block = { uint8 qs[32]; f16 d (little
+ *           endian) }; code i of qs[j] (bits 2i..2i+1) is element 4j+i of
+ *           the block.  The caller keeps ownership; the bytes are copied.
+ *   N, K    weight rows and inner dimension; N >= 1, K >= 128, K % 128 == 0,
+ *           N*K < 2^40.  Else TQ2_ESHAPE.
+ *   out     receives the handle (set to NULL on failure).
+ *   stream  used for the copy and the repack kernel; the call synchronizes
+ *           it before returning, so `aos` may be freed afterwards.
+ *
+ * Device layout behind the handle ("SoA"): a code plane uint8[N][K/4]
+ * holding each row's qs bytes in K order, and a scale plane uint16[N][K/128]
+ * of f16 bits.  Codes are not validated: code 3 decodes as +2 (3-1).
+ */
+TQ2_API tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, void* stream);
+
+/* Release the handle and its device memory (NULL is accepted).  The caller
+ * must make sure no work that reads it is still pending. */
+TQ2_API tq2_status tq2_free(tq2_handle h);
+
+/* Shape of a handle. */
+TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
+
+/*
+ * tq2_gemm -- out[m,n] = sum_k x[m,k] * W[n,k].
+ * Passage: encode_gemm_tq2(&handle, &input, &mut out, m, n, k) and its CPU
+ * reference ("oxibonsai-kernels 0.2.1, tests_gemm_tq2.rs",
+ * test_encode_gemm_tq2_matches_reference: out is row-major [M][N]).
+ *
+ *   x       DEVICE float[M][K], row-major, 16-byte aligned.
+ *   out     DEVICE float[M][N], row-major, overwritten.
+ *   M       >= 1 (M == 0 is a no-op returning TQ2_OK).
+ *   N, K    must equal the handle's shape, else TQ2_ESHAPE.
+ *   stream  asynchronous on this stream.  Internal scratch (f16 copies of
+ *           x) is taken from the stream-ordered allocator of the current
+ *           device and released on the same stream.
+ *
+ * M <= 16 runs the skinny kernel: f32 activations split exactly into two
+ * f16 terms, f32 accumulation; |error| <= 1e-3 at K <= 4096 for unit-scale
+ * data.  M > 16 runs the tensor-core kernel: activations rounded to f16
+ * (nearest-even), weights exact in f16, f32 accumulation;
+ * |error| <= 1e-2 * sum_k |x[m,k] W[n,k]|.
+ */
+TQ2_API tq2_status tq2_gemm(tq2_handle h, const float* x, float* out, int64_t M, int64_t N, int64_t K,
+                    void* stream);
+
+/* tq2_gemm with an explicit kernel choice (tq2_path).  TQ2_PATH_SKINNY
+ * requires M <= 16 (else TQ2_ESHAPE). */
+TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64_t M, int64_t N, int64_t K,
+                         int path, void* stream);
+
+/*
+ * tq2_unpack -- rebuild the AoS bytes from the device planes (round trip of
+ * tq2_upload).  aos_out: HOST buffer of N*(K/128)*34 bytes.  Synchronous.
+ */
+TQ2_API tq2_status tq2_unpack(tq2_handle h, void* aos_out, void* stream);
+
+/*
+ * tq2_dequant_f16 -- W[n,k] = (c-1)*d as f16 bits, exact (code x scale is
+ * representable in f16; "oxibonsai-kernels 0.2.1, tests_gemm_tq2.rs", the
+ * v10 parity test notes that f16 staging of code x scale is exact).
+ *   w   DEVICE uint16[N][K], overwritten.  Debug / test export.
+ */
+TQ2_API tq2_status tq2_dequant_f16(tq2_handle h, uint16_t* w, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Binary low-rank layer (blr)                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * blr_expand_bits -- sign bitmap to an f16 +-1 plane (bit-exact).
+ * Passage: kernels expand_n / expand_t ("cortiq-engine 0.8.43,
+ * train_mm.rs"): bitmap [rows][r/32] u32, bit j of word w is rank 32w+j,
+ * a set bit is +1.0, a clear bit -1.0.
+ *   bits       DEVICE uint32[rows][r/32].
+ *   plane_f16  DEVICE uint16[rows][r] (transpose == 0) or [r][rows]
+ *              (transpose != 0), f16 bits, overwritten.
+ *   rows >= 1; r >= 32, r % 32 == 0.
+ */
+TQ2_API tq2_status blr_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, uint16_t* plane_f16,
+                           int transpose, void* stream);
+
+/*
+ * blr_forward -- one path of the binary low-rank layer, forward.
+ * Passage: blr_forward and the module doc ("cortiq-engine 0.8.43,
+ * train_mm.rs"):  a = (x.g) S_V,  c = (a.l) S_U^T,  y = h.c
+ * (elementwise products broadcast over tokens).
+ *
+ *   bits_u  DEVICE uint32[d_out][r/32]  (S_U, [d_out][r])
+ *   bits_v  DEVICE uint32[d_in][r/32]   (S_V, [d_in][r])
+ *   h       DEVICE float[d_out];  l  DEVICE float[r];  g  DEVICE float[d_in]
+ *   x       DEVICE float[T][d_in]
+ *   y       DEVICE float[T][d_out], overwritten
+ *   a_save  DEVICE float[T][r], overwritten with a (needed by blr_backward)
+ *   c_save  DEVICE float[T][d_out] overwritten with c, or NULL (then
+ *           blr_backward recomputes c from a_save)
+ *   T >= 1; d_in, d_out >= 1 and multiples of 32; r >= 128, r % 128 == 0
+ *   (the page requires a multiple of 128).  Else TQ2_ESHAPE.
+ * The activations x.g and a.l are staged to f16 (nearest-even); the GEMMs
+ * accumulate in f32.  Scratch comes from the stream-ordered allocator.
+ */
+TQ2_API tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h,
+                       const float* l, const float* g, const float* x, float* y,
+                       float* a_save, float* c_save, int64_t T, int64_t d_in, int64_t d_out,
+                       int64_t r, void* stream);
+
+/*
+ * blr_backward -- one path of the binary low-rank layer, backward.
+ * Passage: blr_backward and the module doc ("cortiq-engine 0.8.43,
+ * train_mm.rs"):
+ *   dh += sum_t dy.c     b   = (dy.h) S_U     dl += sum_t a.b
+ *   dx' = (b.l) S_V^T    dg += sum_t x.dx'    dx  = g.dx'
+ *
+ *   x, dy         DEVICE float[T][d_in], float[T][d_out]
+ *   a_save        DEVICE float[T][r] from blr_forward on the same x
+ *   c_save        DEVICE float[T][d_out] from blr_forward, or NULL (recompute)
+ *   dx            DEVICE float[T][d_in], overwritten
+ *   dh, dl, dg    DEVICE float[d_out], float[r], float[d_in]; ACCUMULATED
+ *                 (+=) as on the page; the caller zeroes them.
+ *   gscale        power of two (1.0 allowed) multiplying the gradients while
+ *                 they are staged in f16, divided back out after each GEMM
+ *                 (the page keeps gradients out of the f16 subnormals this
+ *                 way).  Else TQ2_EINVAL.
+ * Column sums use a fixed reduction order (deterministic run to run).
+ * Shape rules as blr_forward.
+ */
+TQ2_API tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h,
+                        const float* l, const float* g, const float* x, const float* dy,
+                        const float* a_save, const float* c_save, float* dx, float* dh,
+                        float* dl, float* dg, int64_t T, int64_t d_in, int64_t d_out,
+                        int64_t r, float gscale, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ2_GB300_H */

@@ -27,14 +27,31 @@ MASK64 = (1 << 64) - 1
 # --------------------------------------------------------------------------
 # the pages' own generators (small sizes; pure Python)
 # --------------------------------------------------------------------------
-def lcg_codes(count, seed=0x12345678):
-    """``count`` ternary codes from the pages' LCG, in generation order."""
+def lcg_codes_loop(count, seed=0x12345678):
+    """``count`` ternary codes from the pages' LCG, in generation order (loop)."""
     s = seed & 0xFFFFFFFF
     out = np.empty(count, dtype=np.uint8)
     for i in range(count):
         s = (s * 1664525 + 1013904223) & 0xFFFFFFFF
         out[i] = (s >> 16) % 3
     return out
+
+
+def lcg_codes(count, seed=0x12345678):
+    """The same codes as :func:`lcg_codes_loop`, by the closed form of the
+    recurrence: state ``n`` is ``a^n s0 + c (1 + a + ... + a^(n-1))`` mod 2^32
+    (numpy's uint64 products and sums wrap mod 2^64, which keeps mod 2^32)."""
+    count = int(count)
+    if count == 0:
+        return np.empty(0, dtype=np.uint8)
+    a, c = np.uint64(1664525), np.uint64(1013904223)
+    powers = np.empty(count + 1, dtype=np.uint64)
+    powers[0] = 1
+    powers[1:] = a
+    powers = np.cumprod(powers)                     # a^0 .. a^count (mod 2^64)
+    geo = np.cumsum(powers[:-1])                    # 1 + a + ... + a^(n-1), n = 1..count
+    states = (powers[1:] * np.uint64(seed & 0xFFFFFFFF) + c * geo) & np.uint64(0xFFFFFFFF)
+    return ((states >> np.uint64(16)) % np.uint64(3)).astype(np.uint8)
 
 
 def xorshift_uniform(n, seed, scale):

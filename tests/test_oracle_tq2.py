@@ -148,3 +148,8 @@ def test_rejects_bad_shapes():
         tq2.parse_aos(b"\0" * 34, 1, 100)
     with pytest.raises(ValueError):
         tq2.parse_aos(b"\0" * 33, 1, 128)
+
+
+def test_vectorised_lcg_equals_the_page_loop():
+    for seed in (0x12345678, 0xDEADBEEF ^ 3072, 0x9E3779B1 ^ (40 << 8) ^ 256):
+        assert np.array_equal(synth.lcg_codes(5000, seed), synth.lcg_codes_loop(5000, seed))
