@@ -105,7 +105,7 @@ class Clocks:
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         busy = sorted(sm)[len(sm) // 4:] if sm else []
         return {"sm_mhz": float(np.median(busy)) if busy else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
@@ -121,14 +121,15 @@ def time_graph(torch, fn, steps, warmup, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         fn()
-    for _ in range(warmup):
-        g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):            # replays run on the current stream
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
     e1.synchronize()
     return e0.elapsed_time(e1) / 1e3, g
 
@@ -159,8 +160,9 @@ def run_gemv(torch, bpw, args, stream, dev):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         step()
-    for _ in range(max(3, args.warmup)):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
     torch.cuda.synchronize()
     return dict(ws=ws, x=x, out=out, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
 
@@ -308,10 +310,11 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
     e1.synchronize()
     clk = clocks.stop()
     secs = e0.elapsed_time(e1) / 1e3
