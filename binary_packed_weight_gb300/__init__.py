@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
-    "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
+    "tq2_gemm_skinny_static", "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
     "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -34,6 +34,7 @@ _SIGS = {
     "tq2_shape": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "tq2_gemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "tq2_gemm_path": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "tq2_gemm_skinny_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "tq2_unpack": (_I, [_P, _P, _P]),
     "tq2_dequant_f16": (_I, [_P, _P, _P]),
     "blr_expand_bits": (_I, [_P, _I64, _I64, _P, _I, _P]),
@@ -122,6 +123,15 @@ def tq2_gemm(w, x, out, stream=None):
 def tq2_gemm_path(w, x, out, path, stream=None):
     M, K = x.shape
     _check(load().tq2_gemm_path(w.handle, _ptr(x), _ptr(out), M, w.N, K, path, _stream(stream)), "tq2_gemm_path")
+    return out
+
+
+def tq2_gemm_skinny_static(w, x, out, stream=None):
+    """Skinny GEMM (M <= 16) that allocates nothing: its scratch is a fixed
+    device array inside the library (see include/tq2.h)."""
+    M, K = x.shape
+    _check(load().tq2_gemm_skinny_static(w.handle, _ptr(x), _ptr(out), M, w.N, K, _stream(stream)),
+           "tq2_gemm_skinny_static")
     return out
 
 

@@ -16,6 +16,9 @@
 // enough into hi = f16(x) and lo = f16(x - hi) (two B columns), which leaves
 // a relative residual below 2^-21.  Weights enter the MMA as (c-1) in f16
 // (exact); the block scale d multiplies the f32 block partial afterwards.
+#include <mutex>
+
+#include "../../include/tq2.h"
 #include "ptx.cuh"
 #include "tq2_internal.h"
 
@@ -292,3 +295,76 @@ unsigned int read_clear_dev_error_skinny(cudaStream_t st) {
 }
 
 }  // namespace tq2
+
+// --------------------------------------------------------------------------
+// Allocation-free variant of the skinny GEMM.
+//
+// Some callers must not allocate device memory while they run a GEMM: a
+// plugin or custom-op interface that forbids allocation inside its enqueue
+// call, a serving process that reserved all device memory up front, or a
+// real-time loop where an allocator call could stall or fail.  For them,
+// tq2_gemm_skinny_static keeps its scratch (the staged hi/lo f16 fragments
+// of x) in the fixed device array below instead of asking the stream-ordered
+// allocator, and calls no allocating routine at all.
+// --------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;     // 1 MiB per device
+// Lives in every GPU that loads this library until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+std::mutex g_static_scratch_mutex;
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (host code only sees a stand-in for the array, never its device
+// address, so the address must come from cudaGetSymbolAddress).
+cudaError_t static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+    if (!g_static_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" TQ2_API tq2_status tq2_gemm_skinny_static(tq2_handle h, const float* x, float* out, int64_t M,
+                                                     int64_t N, int64_t K, void* stream) {
+    if (!h) return (tq2_status)tq2::set_error(TQ2_EINVAL, "tq2_gemm_skinny_static: null handle");
+    if (M == 0) return TQ2_OK;
+    if (!x || !out) return (tq2_status)tq2::set_error(TQ2_EINVAL, "tq2_gemm_skinny_static: null pointer");
+    if (M < 0 || M > 16)
+        return (tq2_status)tq2::set_error(TQ2_ESHAPE, "tq2_gemm_skinny_static: need 1 <= M <= 16 (M=%lld)", (long long)M);
+    if (N != h->N || K != h->K)
+        return (tq2_status)tq2::set_error(TQ2_ESHAPE, "tq2_gemm_skinny_static: (N,K)=(%lld,%lld) but the handle holds (%lld,%lld)",
+                                     (long long)N, (long long)K, (long long)h->N, (long long)h->K);
+    if ((reinterpret_cast<uintptr_t>(x) & 15) != 0)
+        return (tq2_status)tq2::set_error(TQ2_EINVAL, "tq2_gemm_skinny_static: x must be 16-byte aligned");
+    const size_t need = tq2::skinny_scratch_bytes(M, K);
+    if (need > kStaticScratchBytes)
+        return (tq2_status)tq2::set_error(TQ2_ESHAPE,
+                                     "tq2_gemm_skinny_static: needs %zu bytes of scratch for M=%lld K=%lld, above the "
+                                     "fixed %zu-byte area (ceil(M/4)*K*16 must be <= %zu)",
+                                     need, (long long)M, (long long)K, kStaticScratchBytes, kStaticScratchBytes);
+    void* scratch = nullptr;
+    cudaError_t e = static_scratch(&scratch);
+    if (e != cudaSuccess)
+        return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    // Every element of the scratch that the GEMM reads is written first by the
+    // staging kernel of the same call, so nothing needs clearing.
+    e = tq2::launch_skinny(h->codes, h->scales, x, out, (int)M, (int)N, (int)K, scratch,
+                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: launch: %s", cudaGetErrorString(e));
+    return TQ2_OK;
+}

@@ -157,6 +157,31 @@ TQ2_API tq2_status tq2_unpack(tq2_handle h, void* aos_out, void* stream);
  */
 TQ2_API tq2_status tq2_dequant_f16(tq2_handle h, uint16_t* w, void* stream);
 
+/*
+ * tq2_gemm_skinny_static -- the skinny GEMM (M <= 16) without any device
+ * allocation.  The pages have no counterpart to this call; it exists for
+ * callers that must not allocate while they run a GEMM: plugin or custom-op
+ * interfaces that forbid allocation inside their enqueue call, serving
+ * processes that reserve all device memory up front, and real-time loops in
+ * which an allocator call could stall or fail.
+ *
+ *   Same arguments and result as tq2_gemm with M <= 16 (the skinny kernel).
+ *   Scratch: a fixed 1 MiB device array inside the library (one per GPU that
+ *   loads it, held until the process exits) holds the staged f16 fragments
+ *   of x, ceil(M/4)*K*16 bytes; larger requests (for example K > 16384 at
+ *   M = 16, K > 65536 at M <= 4) return TQ2_ESHAPE.  No cudaMalloc,
+ *   cudaFree or stream-ordered allocation is made.
+ *   The first call on a device looks up the array's device address on the
+ *   current device (cudaGetSymbolAddress) and caches it; make that first
+ *   call before any stream capture.
+ *   Every call shares the one array: calls whose work may overlap on the GPU
+ *   (different streams, or different threads without ordering) race on it.
+ *   Nothing in it needs clearing between calls: each call writes every byte
+ *   it later reads.
+ */
+TQ2_API tq2_status tq2_gemm_skinny_static(tq2_handle h, const float* x, float* out, int64_t M, int64_t N,
+                                          int64_t K, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Binary low-rank layer (blr)                                               */
 /* ------------------------------------------------------------------------ */

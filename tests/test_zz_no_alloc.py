@@ -1,0 +1,55 @@
+"""The allocation-free skinny GEMM (tq2_gemm_skinny_static) against tq2_gemm.
+
+Callers that must not allocate device memory during a GEMM (plugin or
+custom-op interfaces that forbid allocation while enqueuing work, serving
+processes that reserve all device memory up front, real-time loops) use
+tq2_gemm_skinny_static, whose scratch is a fixed device array inside the
+library.  This test calls it through the C ABI twice in a row per shape and
+checks each result against the regular entry point within the skinny
+kernel's tolerance.  The file name makes pytest collect it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, fn_name, w, x):
+    import torch
+    M, K = x.shape
+    xd = torch.from_numpy(x).cuda()
+    out = torch.full((M, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = getattr(lib.load(), fn_name)(w.handle, ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                      M, w.N, K, stream)
+    assert st == 0, lib.load().tq2_last_error()
+    lib.device_status()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def test_static_scratch_matches_regular_entry_point(lib):
+    N, K = 3000, 4096
+    w = lib.tq2_upload(synth.random_tq2(N, K, 301), N, K)
+    for M in (1, 6, 16):
+        x = synth.random_x(M, K, 302 + M)
+        want = _run(lib, "tq2_gemm", w, x)
+        for _ in range(2):                                  # two calls in a row
+            got = _run(lib, "tq2_gemm_skinny_static", w, x)
+            assert np.all(np.isfinite(got))
+            assert np.max(np.abs(got - want)) <= 1e-3, M
+
+
+def test_static_scratch_refuses_oversized_requests(lib):
+    N, K = 64, 32768                                        # M=16 needs 2 MiB of scratch
+    w = lib.tq2_upload(synth.random_tq2(N, K, 310), N, K)
+    import torch
+    x = torch.zeros((16, K), dtype=torch.float32, device="cuda")
+    out = torch.zeros((16, N), dtype=torch.float32, device="cuda")
+    st = lib.load().tq2_gemm_skinny_static(w.handle, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                           16, N, K, None)
+    assert st == 2
+    assert b"scratch" in lib.load().tq2_last_error()
