@@ -172,6 +172,11 @@ tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64_t M, in
     cudaStream_t st = S(stream);
     if (path == TQ2_PATH_SKINNY) {
         if (M > 16) return fail(TQ2_ESHAPE, "tq2_gemm: skinny kernel needs M <= 16");
+        if (M <= tq2::GEMV_MAX_M) {          // fused single-kernel GEMV, no scratch
+            cudaError_t e = tq2::launch_gemv(h->codes, h->scales, x, out, (int)M, (int)N, (int)K, st);
+            if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm: gemv launch");
+            return TQ2_OK;
+        }
         void* scratch = nullptr;
         cudaError_t e = cudaMallocAsync(&scratch, tq2::skinny_scratch_bytes(M, K), st);
         if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm: scratch");

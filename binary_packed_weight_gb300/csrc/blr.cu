@@ -1,14 +1,35 @@
 // blr.cu -- binary low-rank layer ("cortiq-engine 0.8.43, src/gpu_wgpu/
-// train_mm.rs"): sign-bitmap expansion and the layer's forward / backward.
+// train_mm.rs"): sign-bitmap expansion and one path's forward / backward.
+//
+//   W = diag(h) S_U diag(l) S_V^T diag(g)         (module doc)
+//   forward   a = (x.g) S_V      c = (a.l) S_U^T      y = h.c
+//   backward  dh += sum_t dy.c   b = (dy.h) S_U       dl += sum_t a.b
+//             dx' = (b.l) S_V^T  dg += sum_t x.dx'    dx = g.dx'
 //
 // Bitmap convention (kernels expand / expand_n / expand_t on that page):
 // bits [rows][r/32] u32, bit j of word w is rank 32w + j, a set bit is +1.
+//
+// GPU mapping.  Each product is one tcgen05 GEMM D[t,n] = sum_k act[t,k] P[n,k]
+// over a sign plane P decoded from bits on chip (umma_core.cuh, DecSign):
+//   a  : act = f16(x.g)            P = S_V^T  (bits of S_V transposed, [r][d_in/32]),  K = d_in
+//   c  : act = f16(a.l)            P = S_U    (bits_u as given),                        K = r
+//   b  : act = f16(dy.h.gs)        P = S_U^T  (bits of S_U transposed),                 K = d_out
+//   dx': act = f16(b.l.gs)         P = S_V    (bits_v as given),                        K = r
+// The elementwise factors are fused into the f16 staging passes (as the
+// page's cvt kernels do), y = h.c and dx = g.dx' into the GEMM epilogues, and
+// the column sums dh, dl, dg are two-pass reductions in a fixed order
+// (partials per token tile or chunk, then an ordered sum), so every result is
+// deterministic.  gs (a power of two) keeps staged gradients away from the
+// f16 subnormals; the GEMMs divide it back out.
+#include <cmath>
+
 #include "../../include/tq2.h"
-#include "ptx.cuh"
 #include "tq2_internal.h"
+#include "umma_core.cuh"
 
 namespace tq2 {
 
+// ------------------------------------------------------------ expansion ----
 // One thread per output element; f16 +-1 = 0x3C00 with the sign bit set
 // for a clear bit.
 __global__ void expand_bits_kernel(const uint32_t* __restrict__ bits, int64_t rows, int64_t r,
@@ -34,6 +55,119 @@ cudaError_t launch_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, ui
     return cudaGetLastError();
 }
 
+// -------------------------------------------------------- bit transpose ----
+// bits [rows][r/32] -> out [r][rows/32]: warp per 32x32 bit tile; lane i holds
+// row 32*rg+i's word kw; the ballot over bit b gives column 32*kw+b's 32 bits.
+__global__ void bits_transpose_kernel(const uint32_t* __restrict__ bits, uint32_t* __restrict__ out, int rows,
+                                      int r) {
+    const int wpr = r / 32, opr = rows / 32;
+    const int64_t tile = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (tile >= (int64_t)opr * wpr) return;
+    const int lane = threadIdx.x & 31;
+    const int rg = (int)(tile / wpr), kw = (int)(tile % wpr);
+    const uint32_t w = bits[(int64_t)(32 * rg + lane) * wpr + kw];
+    uint32_t mine = 0;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+        const uint32_t m = __ballot_sync(0xffffffffu, (w >> b) & 1u);
+        if (lane == b) mine = m;
+    }
+    out[(int64_t)(32 * kw + lane) * opr + rg] = mine;
+}
+
+// ------------------------------------------------------------- staging ----
+// dst[t][k] f16 = f16((src[t][k] * col[k]) * scale) in the 32-group pair
+// order of DecSign (position 2p = element p, 2p+1 = element p+16).  One
+// thread per 32-element group.
+__global__ void stage32_kernel(const float* __restrict__ src, const float* __restrict__ col, float scale,
+                               uint32_t* __restrict__ dst, int64_t T, int64_t Kd) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t groups = T * (Kd / 32);
+    for (int64_t gi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gi < groups;
+         gi += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = gi / (Kd / 32), k0 = (gi % (Kd / 32)) * 32;
+        const float4* s4 = reinterpret_cast<const float4*>(src + t * Kd + k0);
+        float e[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = s4[i];
+            e[4 * i] = v.x; e[4 * i + 1] = v.y; e[4 * i + 2] = v.z; e[4 * i + 3] = v.w;
+        }
+        if (col) {
+            const float4* c4 = reinterpret_cast<const float4*>(col + k0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = c4[i];
+                e[4 * i] *= v.x; e[4 * i + 1] *= v.y; e[4 * i + 2] *= v.z; e[4 * i + 3] *= v.w;
+            }
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+            const __half2 h = __floats2half2_rn(e[p] * scale, e[p + 16] * scale);
+            o[p] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst + (t * Kd + k0) / 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+}
+
+// Sum of S split-K partials [S][T][r] (fixed order) times `oscale`; writes the
+// f32 result (if res) and the 32-group staged f16 of result * col * scale; and,
+// if other/colpart are given, colpart[chunk][k] = sum over the chunk's tokens
+// of result * other (chunk = blockIdx.y, TC tokens per chunk).  Thread per
+// column k (blockDim.x = 256 columns per block, grid.x = ceil(r/256)).
+constexpr int FIN_TC = 32;
+__global__ void finish_splitk_kernel(const float* __restrict__ part, int S, int T, int r, float oscale,
+                                     float* __restrict__ res, const float* __restrict__ col, float scale,
+                                     uint16_t* __restrict__ dst16, const float* __restrict__ other,
+                                     float* __restrict__ colpart) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= r) return;
+    const int t0 = blockIdx.y * FIN_TC, t1 = min(t0 + FIN_TC, T);
+    // position of element k in the 32-group pair order
+    const int g0 = k & ~31, e = k & 31;
+    const int pos = g0 + (e < 16 ? 2 * e : 2 * (e - 16) + 1);
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t) {
+        float v = 0.f;
+        for (int s = 0; s < S; ++s) v += part[((int64_t)s * T + t) * r + k];
+        v *= oscale;
+        if (res) res[(int64_t)t * r + k] = v;
+        dst16[(int64_t)t * r + pos] = __half_as_ushort(__float2half_rn(v * col[k] * scale));
+        if (colpart) acc = fmaf(v, other[(int64_t)t * r + k], acc);
+    }
+    if (colpart) colpart[(int64_t)blockIdx.y * r + k] = acc;
+}
+
+// colpart[chunk][n] = sum over the chunk's tokens of A[t][n] * B[t][n].
+__global__ void colsum_prod_kernel(const float* __restrict__ A, const float* __restrict__ B, int T, int n,
+                                   float* __restrict__ colpart) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= n) return;
+    const int t0 = blockIdx.y * FIN_TC, t1 = min(t0 + FIN_TC, T);
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t) acc = fmaf(A[(int64_t)t * n + j], B[(int64_t)t * n + j], acc);
+    colpart[(int64_t)blockIdx.y * n + j] = acc;
+}
+
+// out[n] += sum_c colpart[c][n], c in order.
+__global__ void colsum_finish_kernel(const float* __restrict__ colpart, int chunks, int n, float* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= n) return;
+    float s = 0.f;
+    for (int c = 0; c < chunks; ++c) s += colpart[(int64_t)c * n + j];
+    out[j] += s;
+}
+
 unsigned int read_clear_dev_error_blr(cudaStream_t st) {
     unsigned int v = 0, z = 0;
     if (cudaMemcpyFromSymbolAsync(&v, g_dev_error, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -43,10 +177,103 @@ unsigned int read_clear_dev_error_blr(cudaStream_t st) {
     return v;
 }
 
+// ---------------------------------------------------------- host pieces ----
+namespace {
+
+struct Scratch {
+    char* base = nullptr;
+    size_t off = 0;
+    template <class T>
+    T* take(size_t n) {
+        T* p = reinterpret_cast<T*>(base + off);
+        off += (n * sizeof(T) + 255) & ~size_t(255);
+        return p;
+    }
+};
+
+int sm_count() {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+int pick_splits(int R, int T, int K, int BN) {
+    const int tiles = ((R + UM_BM - 1) / UM_BM) * ((T + BN - 1) / BN);
+    const int nk = K / UM_BK;
+    int s = (sm_count() + tiles - 1) / tiles;
+    if (s > 8) s = 8;
+    if (s > nk) s = nk;
+    return s < 1 ? 1 : s;
+}
+
+cudaError_t transpose_bits(const uint32_t* bits, uint32_t* out, int rows, int r, cudaStream_t st) {
+    const int64_t tiles = (int64_t)(rows / 32) * (r / 32);
+    bits_transpose_kernel<<<(unsigned)((tiles + 7) / 8), 256, 0, st>>>(bits, out, rows, r);
+    return cudaGetLastError();
+}
+
+cudaError_t stage32(const float* src, const float* col, float scale, void* dst, int T, int Kd, cudaStream_t st) {
+    const int64_t groups = (int64_t)T * (Kd / 32);
+    int64_t blocks = (groups + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(stage32_kernel, dim3((unsigned)blocks), dim3(256), 0, st, src, col, scale,
+                      reinterpret_cast<uint32_t*>(dst), (int64_t)T, (int64_t)Kd);
+}
+
+cudaError_t colsum_finish(const float* colpart, int chunks, int n, float* out, cudaStream_t st) {
+    return launch_pdl(colsum_finish_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, colpart, chunks, n,
+                      out);
+}
+
+// a = (x.g) S_V  (split K, partials summed by finish, which also stages a.l)
+cudaError_t forward_a(const uint32_t* bits_vT, const float* x, const float* g, const float* l, float* a_save,
+                      void* al16, int T, int d_in, int r, Scratch& sc, cudaStream_t st) {
+    void* xg16 = sc.take<uint16_t>((size_t)T * d_in);
+    cudaError_t e = stage32(x, g, 1.0f, xg16, T, d_in, st);
+    if (e != cudaSuccess) return e;
+    const int BN = umma_pick_bn(T);
+    const int S = pick_splits(r, T, d_in, BN);
+    float* part = sc.take<float>((size_t)S * T * r);
+    DecSign dec{bits_vT, (int64_t)d_in / 32};
+    EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
+    e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, xg16, T, r, d_in, BN, S, st);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(finish_splitk_kernel, dim3((unsigned)((r + 255) / 256), (unsigned)((T + FIN_TC - 1) / FIN_TC)),
+                      dim3(256), 0, st, (const float*)part, S, T, r, 1.0f, a_save, l, 1.0f,
+                      reinterpret_cast<uint16_t*>(al16), (const float*)nullptr, (float*)nullptr);
+}
+
+}  // namespace
 }  // namespace tq2
 
+// ---------------------------------------------------------------- C ABI ----
 namespace {
-tq2_status blr_fail(tq2_status st, const char* msg) { return (tq2_status)tq2::set_error(st, "%s", msg); }
+using namespace tq2;
+
+tq2_status blr_fail(tq2_status st, const char* msg) { return (tq2_status)set_error(st, "%s", msg); }
+
+tq2_status check_shapes(const char* who, int64_t T, int64_t d_in, int64_t d_out, int64_t r) {
+    if (T < 1 || d_in < 64 || d_out < 64 || r < 128 || d_in % 64 || d_out % 64 || r % 128)
+        return (tq2_status)set_error(TQ2_ESHAPE,
+                                     "%s: need T >= 1, d_in and d_out multiples of 64, r a multiple of 128 "
+                                     "(T=%lld d_in=%lld d_out=%lld r=%lld)",
+                                     who, (long long)T, (long long)d_in, (long long)d_out, (long long)r);
+    const int64_t mx = d_in > d_out ? d_in : d_out;
+    if (T * mx >= ((int64_t)1 << 31) || T * r * 8 >= ((int64_t)1 << 31) || mx > (1 << 20))
+        return (tq2_status)set_error(TQ2_ESHAPE, "%s: problem too large", who);
+    return TQ2_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+tq2_status cuda_status(cudaError_t e, const char* who) {
+    if (e == cudaSuccess) return TQ2_OK;
+    return (tq2_status)set_error(e == cudaErrorMemoryAllocation ? TQ2_ENOMEM : TQ2_ECUDA, "%s: %s", who,
+                                 cudaGetErrorString(e));
+}
+
 }  // namespace
 
 extern "C" {
@@ -55,19 +282,112 @@ tq2_status blr_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, uint16
                            void* stream) {
     if (!bits || !plane_f16) return blr_fail(TQ2_EINVAL, "blr_expand_bits: null pointer");
     if (rows < 1 || r < 32 || r % 32 != 0) return blr_fail(TQ2_ESHAPE, "blr_expand_bits: need rows >= 1, r % 32 == 0");
-    cudaError_t e = tq2::launch_expand_bits(bits, rows, r, plane_f16, transpose, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TQ2_OK : TQ2_ECUDA;
+    return cuda_status(launch_expand_bits(bits, rows, r, plane_f16, transpose, reinterpret_cast<cudaStream_t>(stream)),
+                       "blr_expand_bits");
 }
 
-tq2_status blr_forward(const uint32_t*, const uint32_t*, const float*, const float*, const float*, const float*,
-                       float*, float*, float*, int64_t, int64_t, int64_t, int64_t, void*) {
-    return blr_fail(TQ2_EUNSUPPORTED, "blr_forward: not built yet");
+tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
+                       const float* x, float* y, float* a_save, float* c_save, int64_t T, int64_t d_in, int64_t d_out,
+                       int64_t r, void* stream) {
+    if (!bits_u || !bits_v || !h || !l || !g || !x || !y || !a_save)
+        return blr_fail(TQ2_EINVAL, "blr_forward: null pointer");
+    tq2_status s = check_shapes("blr_forward", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!aligned16(x) || !aligned16(g) || !aligned16(l))
+        return blr_fail(TQ2_EINVAL, "blr_forward: x, g and l must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
+    const size_t bytes = (size_t)r * d_in / 8 + 256 + (size_t)T * d_in * 2 + 256 + (size_t)T * r * 2 + 256 +
+                         (size_t)8 * T * r * 4 + 256;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocAsync(&mem, bytes, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_forward: scratch");
+    Scratch sc{reinterpret_cast<char*>(mem), 0};
+    uint32_t* bits_vT = sc.take<uint32_t>((size_t)r * d_in / 32);
+    void* al16 = sc.take<uint16_t>((size_t)T * r);
+    e = transpose_bits(bits_v, bits_vT, din, ir, st);
+    if (e == cudaSuccess) e = forward_a(bits_vT, x, g, l, a_save, al16, iT, din, ir, sc, st);
+    if (e == cudaSuccess) {
+        DecSign dec{bits_u, (int64_t)r / 32};
+        EpiArgs ep{y, c_save, h, nullptr, nullptr, (int64_t)d_out, 1.0f};
+        e = launch_umma<DecSign, EPI_SCALE>(dec, ep, al16, iT, dout, ir, umma_pick_bn(iT), 1, st);
+    }
+    cudaError_t e2 = cudaFreeAsync(mem, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_forward");
+    return cuda_status(e2, "blr_forward: scratch free");
 }
 
-tq2_status blr_backward(const uint32_t*, const uint32_t*, const float*, const float*, const float*, const float*,
-                        const float*, const float*, const float*, float*, float*, float*, float*, int64_t, int64_t,
-                        int64_t, int64_t, float, void*) {
-    return blr_fail(TQ2_EUNSUPPORTED, "blr_backward: not built yet");
+tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
+                        const float* x, const float* dy, const float* a_save, const float* c_save, float* dx, float* dh,
+                        float* dl, float* dg, int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale,
+                        void* stream) {
+    if (!bits_u || !bits_v || !h || !l || !g || !x || !dy || !a_save || !dx || !dh || !dl || !dg)
+        return blr_fail(TQ2_EINVAL, "blr_backward: null pointer");
+    tq2_status s = check_shapes("blr_backward", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    int ex = 0;
+    if (!(gscale > 0.f) || !std::isfinite(gscale) || std::frexp(gscale, &ex) != 0.5f)
+        return blr_fail(TQ2_EINVAL, "blr_backward: gscale must be a positive power of two");
+    if (!aligned16(dy) || !aligned16(h) || !aligned16(l) || !aligned16(a_save))
+        return blr_fail(TQ2_EINVAL, "blr_backward: dy, h, l and a_save must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
+    const int BN = umma_pick_bn(iT);
+    const int ttiles = (iT + BN - 1) / BN, chunks = (iT + FIN_TC - 1) / FIN_TC;
+    const int64_t mx = d_in > d_out ? d_in : d_out;
+    const size_t bytes = (size_t)r * d_out / 8 + 256 + (size_t)T * mx * 2 + 256 + (size_t)T * r * 2 + 256 +
+                         (size_t)8 * T * r * 4 + 256 + (size_t)(ttiles + chunks + 2) * (mx + r) * 4 * 2 + 1024;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocAsync(&mem, bytes, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_backward: scratch");
+    Scratch sc{reinterpret_cast<char*>(mem), 0};
+    uint32_t* bits_uT = sc.take<uint32_t>((size_t)r * d_out / 32);
+    void* act16 = sc.take<uint16_t>((size_t)T * mx);        // dy.h.gs, then reused
+    void* r16 = sc.take<uint16_t>((size_t)T * r);           // a.l (dh recompute) / b.l.gs
+    float* colp = sc.take<float>((size_t)(ttiles > chunks ? ttiles : chunks) * mx);
+    const float inv_gs = 1.0f / gscale;
+
+    e = transpose_bits(bits_u, bits_uT, dout, ir, st);
+    // dh += sum_t dy.c
+    if (e == cudaSuccess) {
+        if (c_save) {
+            e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 255) / 256), (unsigned)chunks), dim3(256), 0, st,
+                           dy, c_save, iT, dout, colp);
+            if (e == cudaSuccess) e = colsum_finish(colp, chunks, dout, dh, st);
+        } else {                                             // recompute c = (a.l) S_U^T in the GEMM
+            e = stage32(a_save, l, 1.0f, r16, iT, ir, st);
+            if (e == cudaSuccess) {
+                DecSign dec{bits_u, (int64_t)r / 32};
+                EpiArgs ep{nullptr, nullptr, nullptr, dy, colp, (int64_t)d_out, 1.0f};
+                e = launch_umma<DecSign, EPI_COLSUM>(dec, ep, r16, iT, dout, ir, BN, 1, st);
+            }
+            if (e == cudaSuccess) e = colsum_finish(colp, ttiles, dout, dh, st);
+        }
+    }
+    // b = (dy.h.gs) S_U / gs; dl += sum_t a.b; stage b.l.gs
+    if (e == cudaSuccess) e = stage32(dy, h, gscale, act16, iT, dout, st);
+    if (e == cudaSuccess) {
+        const int S = pick_splits(ir, iT, dout, BN);
+        float* part = sc.take<float>((size_t)S * T * r);
+        DecSign dec{bits_uT, (int64_t)d_out / 32};
+        EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
+        e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, act16, iT, ir, dout, BN, S, st);
+        if (e == cudaSuccess)
+            e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 255) / 256), (unsigned)chunks), dim3(256), 0, st,
+                           (const float*)part, S, iT, ir, inv_gs, (float*)nullptr, l, gscale,
+                           reinterpret_cast<uint16_t*>(r16), a_save, colp);
+        if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);
+    }
+    // dx' = (b.l.gs) S_V / gs; dx = g.dx'; dg += sum_t x.dx'
+    if (e == cudaSuccess) {
+        DecSign dec{bits_v, (int64_t)r / 32};
+        EpiArgs ep{dx, nullptr, g, x, colp, (int64_t)d_in, inv_gs};
+        e = launch_umma<DecSign, EPI_SCALE_COLSUM>(dec, ep, r16, iT, din, ir, BN, 1, st);
+        if (e == cudaSuccess) e = colsum_finish(colp, ttiles, din, dg, st);
+    }
+    cudaError_t e2 = cudaFreeAsync(mem, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_backward");
+    return cuda_status(e2, "blr_backward: scratch free");
 }
 
 }  // extern "C"

@@ -49,6 +49,11 @@ cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const fl
                           int N, int K, void* scratch, cudaStream_t st);
 unsigned int read_clear_dev_error_skinny(cudaStream_t st);
 
+// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M (no scratch)
+constexpr int GEMV_MAX_M = 2;
+cudaError_t launch_gemv(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M, int N,
+                        int K, cudaStream_t st);
+
 // tq2_umma.cu
 size_t tensor_scratch_bytes(int64_t M, int64_t K);
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,

@@ -213,8 +213,9 @@ TQ2_API tq2_status blr_expand_bits(const uint32_t* bits, int64_t rows, int64_t r
  *   a_save  DEVICE float[T][r], overwritten with a (needed by blr_backward)
  *   c_save  DEVICE float[T][d_out] overwritten with c, or NULL (then
  *           blr_backward recomputes c from a_save)
- *   T >= 1; d_in, d_out >= 1 and multiples of 32; r >= 128, r % 128 == 0
- *   (the page requires a multiple of 128).  Else TQ2_ESHAPE.
+ *   T >= 1; d_in, d_out multiples of 64; r >= 128, r % 128 == 0 (the page
+ *   requires a multiple of 128).  Else TQ2_ESHAPE.  x, g and l must be
+ *   16-byte aligned (TQ2_EINVAL otherwise).
  * The activations x.g and a.l are staged to f16 (nearest-even); the GEMMs
  * accumulate in f32.  Scratch comes from the stream-ordered allocator.
  */
@@ -241,7 +242,7 @@ TQ2_API tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, c
  *                 (the page keeps gradients out of the f16 subnormals this
  *                 way).  Else TQ2_EINVAL.
  * Column sums use a fixed reduction order (deterministic run to run).
- * Shape rules as blr_forward.
+ * Shape rules as blr_forward; dy, h, l and a_save must be 16-byte aligned.
  */
 TQ2_API tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h,
                         const float* l, const float* g, const float* x, const float* dy,

@@ -1,0 +1,162 @@
+"""GPU parity of the blr layer (bitmap expansion, forward, backward) through
+the C ABI against the f64 oracle.
+
+Bounds ("cortiq-engine 0.8.43, train_mm.rs", test blr_layer_matches_host, and
+DESIGN.md "Tolerances"): relative L2 error < 3e-3 per tensor (the page's
+bound) and, per element, |gpu - oracle| <= 2^-9 * (the absolute-value chain
+of the same expression).  Each output passes through at most two f16
+roundings (2 * 2^-11) plus f32 accumulation over at most 4096 + 512 terms.
+"""
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import to_dev
+from oracle import blr as oblr
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2.0 ** -9
+
+
+def _page_inputs(T=70, d_in=384, d_out=256, r=128, pi=0):
+    """The page's blr test data: rnd-based signs, h in [0.02,0.045], l in [0.5,1],
+    g in [0.1,0.2], x scale 2, dy scale 1e-3."""
+    def signs(rows, seed):
+        return np.where(synth.xorshift_uniform(rows * r, seed, 1.0).reshape(rows, r) >= 0, 1.0, -1.0)
+
+    def pack(S):
+        rows = S.shape[0]
+        b = np.zeros((rows, r // 32), dtype=np.uint32)
+        for k in range(r):
+            b[:, k // 32] |= np.where(S[:, k] > 0, np.uint32(1 << (k % 32)), np.uint32(0))
+        return b
+    su, sv = signs(d_out, 10 + pi), signs(d_in, 20 + pi)
+    return dict(
+        bits_u=pack(su), bits_v=pack(sv),
+        h=(0.02 + np.abs(synth.xorshift_uniform(d_out, 30 + pi, 0.5)) * 0.05).astype(np.float32),
+        l=(0.5 + np.abs(synth.xorshift_uniform(r, 40 + pi, 0.5))).astype(np.float32),
+        g=(0.1 + np.abs(synth.xorshift_uniform(d_in, 50 + pi, 0.5)) * 0.2).astype(np.float32),
+        x=synth.xorshift_uniform(T * d_in, 60, 2.0).reshape(T, d_in),
+        dy=synth.xorshift_uniform(T * d_out, 61, 1e-3).reshape(T, d_out),
+    )
+
+
+def _run(lib, p, gscale=1.0, save_c=True):
+    import torch
+    T, d_in = p["x"].shape
+    d_out, r = p["h"].size, p["l"].size
+    d = {k: to_dev(v) for k, v in p.items()}
+    d["bits_u"] = to_dev(p["bits_u"].view(np.int32))
+    d["bits_v"] = to_dev(p["bits_v"].view(np.int32))
+    f = dict(dtype=torch.float32, device="cuda")
+    y = torch.full((T, d_out), float("nan"), **f)
+    a = torch.full((T, r), float("nan"), **f)
+    c = torch.full((T, d_out), float("nan"), **f) if save_c else None
+    lib.blr_forward(d["bits_u"], d["bits_v"], d["h"], d["l"], d["g"], d["x"], y, a, c)
+    dx = torch.full((T, d_in), float("nan"), **f)
+    dh, dl, dg = torch.zeros(d_out, **f), torch.zeros(r, **f), torch.zeros(d_in, **f)
+    lib.blr_backward(d["bits_u"], d["bits_v"], d["h"], d["l"], d["g"], d["x"], d["dy"], a, c, dx, dh, dl, dg,
+                     gscale=gscale)
+    lib.device_status()
+    out = dict(y=y, a=a, dx=dx, dh=dh, dl=dl, dg=dg)
+    if save_c:
+        out["c"] = c
+    return {k: v.cpu().numpy().astype(np.float64) for k, v in out.items()}
+
+
+def _oracle(p):
+    y, a, c = oblr.forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"])
+    dx, dh, dl, dg, _, _ = oblr.backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"], p["dy"])
+    ya, aa, dxa, _, dha, dla, dga = oblr.abs_chain(p["h"], p["l"], p["g"], p["x"], p["dy"])
+    ca = ya / np.asarray(p["h"], dtype=np.float64)[None, :]
+    return (dict(y=y, a=a, c=c, dx=dx, dh=dh, dl=dl, dg=dg),
+            dict(y=ya, a=aa, c=ca, dx=dxa, dh=dha, dl=dla, dg=dga))
+
+
+def _check(got, want, chain, where):
+    for k, g in got.items():
+        w, ch = want[k], chain[k]
+        assert np.all(np.isfinite(g)), f"{where} {k}: not finite"
+        rel = np.sqrt(np.sum((g - w) ** 2) / max(np.sum(w * w), 1e-300))
+        assert rel < 3e-3, f"{where} {k}: relative L2 error {rel:.3e}"
+        bad = np.abs(g - w) > TOL * ch + 1e-30
+        assert not bad.any(), f"{where} {k}: {bad.sum()} elements above 2^-9 of the abs chain"
+
+
+def test_expand_bits_bit_exact(lib):
+    import torch
+    for rows, r, key in ((256, 128, 1), (40, 96, 2), (3, 32, 3)):
+        bits = synth.sign_bits(rows, r, key)
+        want = oblr.expand_bits(bits, rows, r).astype(np.float16).view(np.uint16)
+        db = to_dev(bits.view(np.int32))
+        for tr in (0, 1):
+            plane = torch.zeros((r, rows) if tr else (rows, r), dtype=torch.int16, device="cuda")
+            lib.blr_expand_bits(db, rows, r, plane, tr)
+            lib.device_status()
+            got = plane.cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, want.T if tr else want), (rows, r, tr)
+
+
+@pytest.mark.parametrize("gscale", [1.0, 1024.0])
+@pytest.mark.parametrize("save_c", [True, False])
+def test_blr_page_shape(lib, gscale, save_c):
+    p = _page_inputs()
+    got = _run(lib, p, gscale=gscale, save_c=save_c)
+    want, chain = _oracle(p)
+    _check(got, want, chain, f"page shape gs={gscale} save_c={save_c}")
+
+
+@pytest.mark.parametrize("T,d_in,d_out,r", [(1, 64, 64, 128), (33, 192, 320, 256), (300, 512, 448, 384)])
+def test_blr_ragged_shapes(lib, T, d_in, d_out, r):
+    p = synth.blr_inputs(T, d_in, d_out, r, 200 + T)
+    got = _run(lib, p, save_c=(T % 2 == 1))
+    want, chain = _oracle(p)
+    _check(got, want, chain, f"T={T} d_in={d_in} d_out={d_out} r={r}")
+
+
+def test_blr_full_size(lib):
+    cfg = synth.BLR
+    p = synth.blr_inputs(cfg["T"], cfg["d_in"], cfg["d_out"], cfg["r"], cfg["key"])
+    got = _run(lib, p, save_c=False)
+    want, chain = _oracle(p)
+    _check(got, want, chain, "T=2048 d=4096 r=512")
+
+
+def test_blr_deterministic_and_accumulating(lib):
+    p = synth.blr_inputs(130, 256, 192, 128, 300)
+    r1 = _run(lib, p, save_c=False)
+    r2 = _run(lib, p, save_c=False)
+    for k in r1:
+        assert np.array_equal(r1[k], r2[k]), k
+    # dh/dl/dg accumulate: a second backward on the same buffers doubles them
+    import torch
+    T, d_in = p["x"].shape
+    d_out, r = p["h"].size, p["l"].size
+    d = {k: to_dev(v) for k, v in p.items() if k not in ("bits_u", "bits_v")}
+    bu, bv = to_dev(p["bits_u"].view(np.int32)), to_dev(p["bits_v"].view(np.int32))
+    f = dict(dtype=torch.float32, device="cuda")
+    y, a = torch.empty((T, d_out), **f), torch.empty((T, r), **f)
+    lib.blr_forward(bu, bv, d["h"], d["l"], d["g"], d["x"], y, a, None)
+    dx = torch.empty((T, d_in), **f)
+    dh, dl, dg = torch.zeros(d_out, **f), torch.zeros(r, **f), torch.zeros(d_in, **f)
+    for _ in range(2):
+        lib.blr_backward(bu, bv, d["h"], d["l"], d["g"], d["x"], d["dy"], a, None, dx, dh, dl, dg)
+    lib.device_status()
+    for k, v in (("dh", dh), ("dl", dl), ("dg", dg)):
+        assert np.array_equal(v.cpu().numpy(), 2 * r1[k].astype(np.float32)), k
+
+
+def test_blr_rejects_bad_arguments(lib):
+    import ctypes
+    import torch
+    L = lib.load()
+    z = torch.zeros(4096, dtype=torch.float32, device="cuda")
+    pz = ctypes.c_void_p(z.data_ptr())
+    # shapes: d_in not a multiple of 64, r not a multiple of 128
+    assert L.blr_forward(pz, pz, pz, pz, pz, pz, pz, pz, None, 4, 96, 64, 128, None) == 2
+    assert L.blr_forward(pz, pz, pz, pz, pz, pz, pz, pz, None, 4, 64, 64, 96, None) == 2
+    assert L.blr_forward(None, pz, pz, pz, pz, pz, pz, pz, None, 4, 64, 64, 128, None) == 1
+    # gscale must be a positive power of two
+    for gs in (3.0, 0.0, -2.0):
+        assert L.blr_backward(pz, pz, pz, pz, pz, pz, pz, pz, None, pz, pz, pz, pz, 4, 64, 64, 128, gs, None) == 1
