@@ -223,6 +223,59 @@ def extra_skinny(torch, bpw, stream, dev, pk, Ms):
     return res
 
 
+def extra_grouped(torch, bpw, ctx, stream, pk):
+    """The same 64 GEMVs as one grouped launch (independent weights, shared x)."""
+    ws, x, N, K, M = ctx["ws"], ctx["x"], ctx["N"], ctx["K"], ctx["M"]
+    outs = [torch.empty((M, N), dtype=torch.float32, device=x.device) for _ in ws]
+    xs = [x] * len(ws)
+
+    def step():
+        bpw.tq2_gemm_grouped(ws, xs, outs, stream=stream.cuda_stream)
+    secs, _ = time_graph(torch, step, 200, 5, stream)
+    t = secs / 200
+    wb = gemv_bytes(N, K) * len(ws)
+    alg = wb + len(ws) * (M * K * 4 + M * N * 4)
+    return dict(us_per_launch=t * 1e6, gemvs_per_launch=len(ws), weight_gbs=wb / t / 1e9,
+                alg_gbs=alg / t / 1e9, hbm_frac=alg / t / 1e9 / pk["hbm"],
+                kernel="tq2_gemv_kernel<1> (table of 64 jobs)")
+
+
+def extra_blr(torch, bpw, stream, dev, pk):
+    """blr layer forward + backward, T=2048 d_in=d_out=4096 r=512 (c recomputed)."""
+    cfg = synth.BLR
+    T, din, dout, r = cfg["T"], cfg["d_in"], cfg["d_out"], cfg["r"]
+    p = synth.blr_inputs(T, din, dout, r, cfg["key"])
+    import numpy as _np
+    d = {k: torch.from_numpy(_np.ascontiguousarray(v)).to(dev) for k, v in p.items() if k not in ("bits_u", "bits_v")}
+    bu = torch.from_numpy(p["bits_u"].view(_np.int32)).to(dev)
+    bv = torch.from_numpy(p["bits_v"].view(_np.int32)).to(dev)
+    f = dict(dtype=torch.float32, device=dev)
+    y, a = torch.empty((T, dout), **f), torch.empty((T, r), **f)
+    dx = torch.empty((T, din), **f)
+    dh, dl, dg = torch.zeros(dout, **f), torch.zeros(r, **f), torch.zeros(din, **f)
+
+    def fwd():
+        bpw.blr_forward(bu, bv, d["h"], d["l"], d["g"], d["x"], y, a, None, stream=stream.cuda_stream)
+
+    def bwd():
+        bpw.blr_backward(bu, bv, d["h"], d["l"], d["g"], d["x"], d["dy"], a, None, dx, dh, dl, dg,
+                         stream=stream.cuda_stream)
+
+    def step():
+        fwd()
+        bwd()
+    tf, _ = time_graph(torch, fwd, 20, 3, stream)
+    tb, _ = time_graph(torch, bwd, 20, 3, stream)
+    ts, _ = time_graph(torch, step, 20, 3, stream)
+    tf, tb, ts = tf / 20, tb / 20, ts / 20
+    flops = 4 * 2.0 * T * din * r                       # four GEMMs of 2*T*4096*512 (c recomputed: a fifth)
+    alg_bytes = 5 * T * din * 4 + 2 * dout * r // 8 + 2 * T * r * 4
+    return dict(fwd_us=tf * 1e6, bwd_us=tb * 1e6, step_us=ts * 1e6, tflops=flops / ts / 1e12,
+                alg_gbs=alg_bytes / ts / 1e9, hbm_frac=alg_bytes / ts / 1e9 / pk["hbm"],
+                tensor_frac=flops / ts / 1e12 / pk["bf16"], algorithmic_bytes=alg_bytes, flops=flops,
+                note="forward + backward of one path; dh from a recomputed c (no c_save)")
+
+
 def extra_large(torch, bpw, stream, dev, pk):
     cfg = synth.LARGE
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
@@ -337,8 +390,12 @@ def main():
         only = set(filter(None, args.only.split(",")))
         if not only or "skinny" in only:
             extra["tq2_skinny_N11008"] = extra_skinny(torch, bpw, stream, dev, pk, (8, 32, 128))
+        if not only or "grouped" in only:
+            extra["tq2_gemv_grouped_64"] = extra_grouped(torch, bpw, ctx, stream, pk)
         if not only or "large" in only:
             extra["tq2_large_M4096_N14336"] = extra_large(torch, bpw, stream, dev, pk)
+        if not only or "blr" in only:
+            extra["blr_T2048_d4096_r512"] = extra_blr(torch, bpw, stream, dev, pk)
 
     if rank != 0:
         return
@@ -358,9 +415,9 @@ def main():
         tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
         roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                   "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv"),
-                  "kernel": "stage_x_frag + tq2_skinny (per GEMV, average over the timed graph replays)",
+                  "kernel": "tq2_gemv_kernel<1> (one launch per GEMV, average over the timed graph replays)",
                   "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"] + " hbm_gbs (copy)"},
-        cpu_baseline=cb, e2e=e2e, gpu_launches=2 * gemvs, clocks=clk, extra=extra,
+        cpu_baseline=cb, e2e=e2e, gpu_launches=gemvs, clocks=clk, extra=extra,
     )
     print(json.dumps(line), flush=True)
     if dist:

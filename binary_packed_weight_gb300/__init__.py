@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
-    "tq2_gemm_skinny_static", "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
+    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
     "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -35,6 +35,7 @@ _SIGS = {
     "tq2_gemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "tq2_gemm_path": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
     "tq2_gemm_skinny_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "tq2_gemm_grouped": (_I, [_P, _P, _P, _I, _I64, _I64, _P]),
     "tq2_unpack": (_I, [_P, _P, _P]),
     "tq2_dequant_f16": (_I, [_P, _P, _P]),
     "blr_expand_bits": (_I, [_P, _I64, _I64, _P, _I, _P]),
@@ -133,6 +134,18 @@ def tq2_gemm_skinny_static(w, x, out, stream=None):
     _check(load().tq2_gemm_skinny_static(w.handle, _ptr(x), _ptr(out), M, w.N, K, _stream(stream)),
            "tq2_gemm_skinny_static")
     return out
+
+
+def tq2_gemm_grouped(ws, xs, outs, stream=None):
+    """G independent GEMVs (M <= 2, same K) in one launch: outs[g] = xs[g] @ W_g^T."""
+    G = len(ws)
+    M, K = xs[0].shape
+    hs = (_P * G)(*[w.handle for w in ws])
+    xp = (_P * G)(*[x.data_ptr() for x in xs])
+    op = (_P * G)(*[o.data_ptr() for o in outs])
+    _check(load().tq2_gemm_grouped(ctypes.cast(hs, _P), ctypes.cast(xp, _P), ctypes.cast(op, _P), G, M, K,
+                                   _stream(stream)), "tq2_gemm_grouped")
+    return outs
 
 
 def tq2_unpack(w, stream=None):

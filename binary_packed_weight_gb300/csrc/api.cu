@@ -204,6 +204,29 @@ tq2_status tq2_gemm(tq2_handle h, const float* x, float* out, int64_t M, int64_t
     return tq2_gemm_path(h, x, out, M, N, K, TQ2_PATH_AUTO, stream);
 }
 
+tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float* const* outs, int G, int64_t M,
+                            int64_t K, void* stream) {
+    if (!hs || !xs || !outs) return fail(TQ2_EINVAL, "tq2_gemm_grouped: null array");
+    if (G < 1 || G > tq2::GEMV_MAX_JOBS) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= G <= %d", tq2::GEMV_MAX_JOBS);
+    if (M < 1 || M > tq2::GEMV_MAX_M) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= M <= %d", tq2::GEMV_MAX_M);
+    tq2::GemvTable tab;
+    tab.njobs = G;
+    tab.K = (int)K;
+    int64_t ctas = 0;
+    for (int g = 0; g < G; ++g) {
+        const tq2_handle h = hs[g];
+        if (!h || !xs[g] || !outs[g]) return fail(TQ2_EINVAL, "tq2_gemm_grouped: null entry %d", g);
+        if (h->K != K) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: entry %d has K=%lld, not %lld", g, (long long)h->K, (long long)K);
+        if ((reinterpret_cast<uintptr_t>(xs[g]) & 15) != 0) return fail(TQ2_EINVAL, "tq2_gemm_grouped: x %d not 16-byte aligned", g);
+        tab.job[g] = tq2::GemvJob{h->codes, h->scales, xs[g], outs[g], (int)h->N, (int)ctas};
+        ctas += (h->N + 15) / 16;
+    }
+    if (ctas >= ((int64_t)1 << 31)) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: too many rows");
+    cudaError_t e = tq2::launch_gemv_table(tab, (int)M, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm_grouped");
+    return TQ2_OK;
+}
+
 tq2_status tq2_unpack(tq2_handle h, void* aos_out, void* stream) {
     if (!h || !aos_out) return fail(TQ2_EINVAL, "tq2_unpack: null pointer");
     const int64_t nblocks = h->N * (h->K / 128);

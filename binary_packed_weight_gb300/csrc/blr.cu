@@ -78,83 +78,100 @@ __global__ void bits_transpose_kernel(const uint32_t* __restrict__ bits, uint32_
 // ------------------------------------------------------------- staging ----
 // dst[t][k] f16 = f16((src[t][k] * col[k]) * scale) in the 32-group pair
 // order of DecSign (position 2p = element p, 2p+1 = element p+16).  One
-// thread per 32-element group.
+// thread per quarter q of a 32-element group: it reads elements 4q..4q+3 and
+// 16+4q..16+4q+3 (two float4) and writes pair words 4q..4q+3 (one uint4), so
+// a warp touches 8 whole 128-byte groups per pair of loads.
 __global__ void stage32_kernel(const float* __restrict__ src, const float* __restrict__ col, float scale,
                                uint32_t* __restrict__ dst, int64_t T, int64_t Kd) {
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t groups = T * (Kd / 32);
-    for (int64_t gi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gi < groups;
-         gi += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t quarters = T * (Kd / 32) * 4;
+    for (int64_t qi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; qi < quarters;
+         qi += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t gi = qi >> 2;
+        const int q = (int)(qi & 3);
         const int64_t t = gi / (Kd / 32), k0 = (gi % (Kd / 32)) * 32;
-        const float4* s4 = reinterpret_cast<const float4*>(src + t * Kd + k0);
-        float e[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = s4[i];
-            e[4 * i] = v.x; e[4 * i + 1] = v.y; e[4 * i + 2] = v.z; e[4 * i + 3] = v.w;
-        }
+        const float* sp = src + t * Kd + k0;
+        float4 lo = *reinterpret_cast<const float4*>(sp + 4 * q);
+        float4 hi = *reinterpret_cast<const float4*>(sp + 16 + 4 * q);
         if (col) {
-            const float4* c4 = reinterpret_cast<const float4*>(col + k0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = c4[i];
-                e[4 * i] *= v.x; e[4 * i + 1] *= v.y; e[4 * i + 2] *= v.z; e[4 * i + 3] *= v.w;
-            }
+            const float4 cl = *reinterpret_cast<const float4*>(col + k0 + 4 * q);
+            const float4 ch = *reinterpret_cast<const float4*>(col + k0 + 16 + 4 * q);
+            lo.x *= cl.x; lo.y *= cl.y; lo.z *= cl.z; lo.w *= cl.w;
+            hi.x *= ch.x; hi.y *= ch.y; hi.z *= ch.z; hi.w *= ch.w;
         }
-        uint32_t o[16];
+        uint32_t o[4];
+        const float l4[4] = {lo.x, lo.y, lo.z, lo.w}, h4[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-            const __half2 h = __floats2half2_rn(e[p] * scale, e[p + 16] * scale);
-            o[p] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(l4[i] * scale, h4[i] * scale);
+            o[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        uint4* d4 = reinterpret_cast<uint4*>(dst + (t * Kd + k0) / 2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        reinterpret_cast<uint4*>(dst + (t * Kd + k0) / 2)[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
 // Sum of S split-K partials [S][T][r] (fixed order) times `oscale`; writes the
 // f32 result (if res) and the 32-group staged f16 of result * col * scale; and,
-// if other/colpart are given, colpart[chunk][k] = sum over the chunk's tokens
-// of result * other (chunk = blockIdx.y, TC tokens per chunk).  Thread per
-// column k (blockDim.x = 256 columns per block, grid.x = ceil(r/256)).
+// if colpart is given, colpart[chunk][k] = sum over the chunk's tokens (in
+// order) of result * other.  Block (32, 8): x = column within a 32-column
+// group, y = token lane; FIN_TC tokens per block.
 constexpr int FIN_TC = 32;
 __global__ void finish_splitk_kernel(const float* __restrict__ part, int S, int T, int r, float oscale,
                                      float* __restrict__ res, const float* __restrict__ col, float scale,
                                      uint16_t* __restrict__ dst16, const float* __restrict__ other,
                                      float* __restrict__ colpart) {
+    __shared__ float red[8][33];
     pdl_wait();
     pdl_launch_dependents();
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= r) return;
-    const int t0 = blockIdx.y * FIN_TC, t1 = min(t0 + FIN_TC, T);
-    // position of element k in the 32-group pair order
-    const int g0 = k & ~31, e = k & 31;
-    const int pos = g0 + (e < 16 ? 2 * e : 2 * (e - 16) + 1);
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int k = blockIdx.x * 32 + tx;
+    const int t0 = blockIdx.y * FIN_TC;
+    const bool kok = k < r;
+    const int pos = (k & ~31) + (tx < 16 ? 2 * tx : 2 * (tx - 16) + 1);
+    const float cs = kok ? col[k] : 0.f;
     float acc = 0.f;
-    for (int t = t0; t < t1; ++t) {
+    for (int t = t0 + ty; t < t0 + FIN_TC && t < T; t += 8) {
+        if (!kok) continue;
         float v = 0.f;
         for (int s = 0; s < S; ++s) v += part[((int64_t)s * T + t) * r + k];
         v *= oscale;
         if (res) res[(int64_t)t * r + k] = v;
-        dst16[(int64_t)t * r + pos] = __half_as_ushort(__float2half_rn(v * col[k] * scale));
+        dst16[(int64_t)t * r + pos] = __half_as_ushort(__float2half_rn(v * cs * scale));
         if (colpart) acc = fmaf(v, other[(int64_t)t * r + k], acc);
     }
-    if (colpart) colpart[(int64_t)blockIdx.y * r + k] = acc;
+    if (colpart) {
+        red[ty][tx] = acc;
+        __syncthreads();
+        if (ty == 0 && kok) {
+            float s2 = 0.f;
+            for (int i = 0; i < 8; ++i) s2 += red[i][tx];
+            colpart[(int64_t)blockIdx.y * r + k] = s2;
+        }
+    }
 }
 
-// colpart[chunk][n] = sum over the chunk's tokens of A[t][n] * B[t][n].
+// colpart[chunk][n] = sum over the chunk's tokens of A[t][n] * B[t][n]
+// (block (32, 8) as finish_splitk_kernel; fixed order).
 __global__ void colsum_prod_kernel(const float* __restrict__ A, const float* __restrict__ B, int T, int n,
                                    float* __restrict__ colpart) {
+    __shared__ float red[8][33];
     pdl_wait();
     pdl_launch_dependents();
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n) return;
-    const int t0 = blockIdx.y * FIN_TC, t1 = min(t0 + FIN_TC, T);
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int j = blockIdx.x * 32 + tx;
+    const int t0 = blockIdx.y * FIN_TC;
     float acc = 0.f;
-    for (int t = t0; t < t1; ++t) acc = fmaf(A[(int64_t)t * n + j], B[(int64_t)t * n + j], acc);
-    colpart[(int64_t)blockIdx.y * n + j] = acc;
+    if (j < n)
+        for (int t = t0 + ty; t < t0 + FIN_TC && t < T; t += 8)
+            acc = fmaf(A[(int64_t)t * n + j], B[(int64_t)t * n + j], acc);
+    red[ty][tx] = acc;
+    __syncthreads();
+    if (ty == 0 && j < n) {
+        float s2 = 0.f;
+        for (int i = 0; i < 8; ++i) s2 += red[i][tx];
+        colpart[(int64_t)blockIdx.y * n + j] = s2;
+    }
 }
 
 // out[n] += sum_c colpart[c][n], c in order.
@@ -214,8 +231,8 @@ cudaError_t transpose_bits(const uint32_t* bits, uint32_t* out, int rows, int r,
 }
 
 cudaError_t stage32(const float* src, const float* col, float scale, void* dst, int T, int Kd, cudaStream_t st) {
-    const int64_t groups = (int64_t)T * (Kd / 32);
-    int64_t blocks = (groups + 255) / 256;
+    const int64_t quarters = (int64_t)T * (Kd / 32) * 4;
+    int64_t blocks = (quarters + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 16;
     if (blocks > cap) blocks = cap;
     return launch_pdl(stage32_kernel, dim3((unsigned)blocks), dim3(256), 0, st, src, col, scale,
@@ -240,8 +257,8 @@ cudaError_t forward_a(const uint32_t* bits_vT, const float* x, const float* g, c
     EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
     e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, xg16, T, r, d_in, BN, S, st);
     if (e != cudaSuccess) return e;
-    return launch_pdl(finish_splitk_kernel, dim3((unsigned)((r + 255) / 256), (unsigned)((T + FIN_TC - 1) / FIN_TC)),
-                      dim3(256), 0, st, (const float*)part, S, T, r, 1.0f, a_save, l, 1.0f,
+    return launch_pdl(finish_splitk_kernel, dim3((unsigned)((r + 31) / 32), (unsigned)((T + FIN_TC - 1) / FIN_TC)),
+                      dim3(32, 8), 0, st, (const float*)part, S, T, r, 1.0f, a_save, l, 1.0f,
                       reinterpret_cast<uint16_t*>(al16), (const float*)nullptr, (float*)nullptr);
 }
 
@@ -351,7 +368,7 @@ tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const fl
     // dh += sum_t dy.c
     if (e == cudaSuccess) {
         if (c_save) {
-            e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 255) / 256), (unsigned)chunks), dim3(256), 0, st,
+            e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
                            dy, c_save, iT, dout, colp);
             if (e == cudaSuccess) e = colsum_finish(colp, chunks, dout, dh, st);
         } else {                                             // recompute c = (a.l) S_U^T in the GEMM
@@ -373,7 +390,7 @@ tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const fl
         EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
         e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, act16, iT, ir, dout, BN, S, st);
         if (e == cudaSuccess)
-            e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 255) / 256), (unsigned)chunks), dim3(256), 0, st,
+            e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
                            (const float*)part, S, iT, ir, inv_gs, (float*)nullptr, l, gscale,
                            reinterpret_cast<uint16_t*>(r16), a_save, colp);
         if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);

@@ -68,14 +68,19 @@ struct GemvSmem {
 };
 
 template <int MT>
-__global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const uint8_t* __restrict__ codes,
-                                                                 const uint16_t* __restrict__ scales,
-                                                                 const float* __restrict__ x,
-                                                                 float* __restrict__ out, int N, int K) {
+__global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const __grid_constant__ GemvTable tab) {
     __shared__ GemvSmem<MT> sm;
+    // the job this CTA belongs to (jobs are laid out back to back in blockIdx.x)
+    int job = 0;
+    while (job + 1 < tab.njobs && (int)blockIdx.x >= tab.job[job + 1].cta0) ++job;
+    const uint8_t* __restrict__ codes = tab.job[job].codes;
+    const uint16_t* __restrict__ scales = tab.job[job].scales;
+    const float* __restrict__ x = tab.job[job].x;
+    float* __restrict__ out = tab.job[job].out;
+    const int N = tab.job[job].N, K = tab.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int n0 = blockIdx.x * 16;
+    const int n0 = ((int)blockIdx.x - tab.job[job].cta0) * 16;
     const int nb = K >> 7;
     const int kb_begin = (nb * warp) / GV_WARPS, kb_end = (nb * (warp + 1)) / GV_WARPS;
     const int rowA = n0 + g, rowB = n0 + g + 8;
@@ -85,8 +90,6 @@ __global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const uint8_t* 
     const uint8_t* pB = codes + (int64_t)(okB ? rowB : 0) * pitch + 8 * t;
     const uint16_t* sA = scales + (int64_t)(okA ? rowA : 0) * nb;
     const uint16_t* sB = scales + (int64_t)(okB ? rowB : 0) * nb;
-
-    pdl_launch_dependents();
 
     // staging role of this lane: word (blk = lane/8, tq = (lane/2)%4, w = lane%2)
     const int st_blk = lane >> 3, st_t = (lane >> 1) & 3, st_w = lane & 1;
@@ -184,6 +187,9 @@ __global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const uint8_t* 
         __syncwarp();
         if (kb0 + GV_CHUNK < kb_end) load_chunk(kb0 + GV_CHUNK);
     }
+    // The next kernel may start launching now: this CTA's loads are done, and
+    // its prefetch cannot delay our (already finished) critical loads.
+    pdl_launch_dependents();
 
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -201,12 +207,21 @@ __global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const uint8_t* 
     }
 }
 
+cudaError_t launch_gemv_table(const GemvTable& tab, int M, cudaStream_t st) {
+    const int ctas = tab.job[tab.njobs - 1].cta0 + (tab.job[tab.njobs - 1].N + 15) / 16;
+    const dim3 grid((unsigned)ctas), block(GV_WARPS * 32);
+    if (M == 1) return launch_pdl(tq2_gemv_kernel<1>, grid, block, 0, st, tab);
+    if (M == 2) return launch_pdl(tq2_gemv_kernel<2>, grid, block, 0, st, tab);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemv(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M, int N,
                         int K, cudaStream_t st) {
-    const dim3 grid((unsigned)((N + 15) / 16)), block(GV_WARPS * 32);
-    if (M == 1) return launch_pdl(tq2_gemv_kernel<1>, grid, block, 0, st, codes, scales, x, out, N, K);
-    if (M == 2) return launch_pdl(tq2_gemv_kernel<2>, grid, block, 0, st, codes, scales, x, out, N, K);
-    return cudaErrorInvalidValue;
+    GemvTable tab;
+    tab.njobs = 1;
+    tab.K = K;
+    tab.job[0] = GemvJob{codes, scales, x, out, N, 0};
+    return launch_gemv_table(tab, M, st);
 }
 
 }  // namespace tq2

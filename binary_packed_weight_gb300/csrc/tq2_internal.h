@@ -49,8 +49,24 @@ cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const fl
                           int N, int K, void* scratch, cudaStream_t st);
 unsigned int read_clear_dev_error_skinny(cudaStream_t st);
 
-// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M (no scratch)
+// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M (no scratch); one launch may
+// run up to GEMV_MAX_JOBS independent GEMVs of the same K and M.
 constexpr int GEMV_MAX_M = 2;
+constexpr int GEMV_MAX_JOBS = 64;
+struct GemvJob {
+    const uint8_t* codes;
+    const uint16_t* scales;
+    const float* x;
+    float* out;
+    int N;
+    int cta0;     // first CTA of this job in the launch
+};
+struct GemvTable {
+    GemvJob job[GEMV_MAX_JOBS];
+    int njobs;
+    int K;
+};
+cudaError_t launch_gemv_table(const GemvTable& tab, int M, cudaStream_t st);
 cudaError_t launch_gemv(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M, int N,
                         int K, cudaStream_t st);
 

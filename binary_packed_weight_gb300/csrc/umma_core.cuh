@@ -7,15 +7,17 @@
 // signs) decoded on chip; act is an f16 activation matrix staged in the K
 // order the decoder emits pairs in.  One CTA computes a 128 (plane rows) x BN
 // (tokens) tile:
-//   * four decoder warps (one plane row per thread = its TMEM lane) write the
-//     decoded f16 pairs into tensor memory with tcgen05.st: the MMA's A
-//     operand never passes through shared memory;
+//   * eight decoder warps (one plane row per thread = its TMEM lane, two
+//     warps per lane quarter splitting each K stage) write the decoded f16
+//     pairs into tensor memory with tcgen05.st: the MMA's A operand never
+//     passes through shared memory;
 //   * one thread issues TMA loads of the activation tile (B operand, 128-byte
 //     swizzle) into a 4-stage shared-memory ring;
-//   * one thread issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) and
-//     frees stages with tcgen05.commit;
-//   * the decoder warps then read the accumulator (tcgen05.ld) and run the
-//     epilogue policy of the call.
+//   * one thread issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
+//     one of two accumulators and frees stages with tcgen05.commit;
+//   * four epilogue warps read the finished accumulator (tcgen05.ld), hand it
+//     back, and run the epilogue policy of the call while the next tile's
+//     MMAs proceed in the other accumulator.
 // All waits are bounded (mbar_wait); a timeout records an error and drains.
 #pragma once
 
@@ -24,16 +26,21 @@
 
 namespace tq2 {
 
-constexpr int UM_BM = 128;       // plane rows per CTA = MMA M
+constexpr int UM_BM = 128;       // plane rows per tile = MMA M
 constexpr int UM_BK = 64;        // K per pipeline stage (128 bytes of f16)
-constexpr int UM_STAGES = 4;
-constexpr int UM_THREADS = 256;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, warps 4-7 decode + epilogue
+constexpr int UM_STAGES = 8;     // ring slots allocated; the launch picks how many it uses
+constexpr int UM_MAX_BN = 256;   // MMA N limit for M = 128
+// warp 0 TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 idle,
+// warps 4-11 decoders (two per TMEM lane quarter, taking alternate stages),
+// warps 12-15 epilogue (one per lane quarter)
+constexpr int UM_THREADS = 512;
 
 struct UmmaBars {
     uint64_t full_b[UM_STAGES];
     uint64_t full_a[UM_STAGES];
     uint64_t empty[UM_STAGES];
-    uint64_t done;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -52,13 +59,28 @@ __device__ __forceinline__ uint2 ldg_u2_nc(const void* p) {
 }
 
 // ---------------------------------------------------------------- decoders ----
-// A decoder turns plane row `row` (valid iff ok) of K-stage i (64 elements)
-// into 32 f16 pairs v[0..31]; column j of the stage holds K positions 2j,2j+1
-// of the permuted order the activations are staged in.
+// A decoder turns K-stage kc (64 elements) of plane row `row` (valid iff ok)
+// into 32 f16 pairs v[0..31]: TMEM column j of the stage holds K positions
+// 2j, 2j+1 of the permuted order the activations are staged in.  Loads go
+// through L1 (the neighbouring stage of the same 32-byte sector is read by
+// the partner decoder warp).
 
-// TQ2 codes: 16 bytes of codes per stage, element e of a 16-element word at
-// bits 2e; pair q = (element q, element q+8); the block scale is folded in:
-// (c-1)*d is exact in f16.  Activations staged with 16-element groups.
+__device__ __forceinline__ uint4 ldg_u4_l1(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_u2_l1(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// TQ2 codes: 16 bytes (four 16-element words) per stage, element e of a word
+// at bits 2e; pair q = (element q, element q+8); the block scale is folded
+// in: (c-1)*d is exact in f16.  Activations staged in 16-element groups.
 struct DecTQ2 {
     const uint8_t* codes;      // [rows][K/4]
     const uint16_t* scales;    // [rows][K/128]
@@ -68,7 +90,7 @@ struct DecTQ2 {
     __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
         Raw r;
         if (ok) {
-            r.c = ldg_u4_nc(codes + (int64_t)row * pitch + (int64_t)kc * 16);
+            r.c = ldg_u4_l1(codes + (int64_t)row * pitch + (int64_t)kc * 16);
             r.d = __ldg(scales + (int64_t)row * nb + kc / 2);
         } else {
             r.c = make_uint4(0u, 0u, 0u, 0u);
@@ -85,23 +107,23 @@ struct DecTQ2 {
             decode_word(words[w], p);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                __half2 h = __hmul2(*reinterpret_cast<__half2*>(&p[q]), d2);
-                v[w * 8 + q] = *reinterpret_cast<uint32_t*>(&h);
+                __half2 hh = __hmul2(*reinterpret_cast<__half2*>(&p[q]), d2);
+                v[w * 8 + q] = *reinterpret_cast<uint32_t*>(&hh);
             }
         }
     }
 };
 
-// Sign bits: 2 words of 32 signs per stage (bit b of word w = element 32w+b,
-// set = +1); pair p = (element p, element p+16) of a word.  Activations
-// staged with 32-element groups.
+// Sign bits: two 32-sign words per stage (bit b = element b of a word, set =
+// +1); pair p = (element p, element p+16).  Activations staged in 32-element
+// groups.
 struct DecSign {
     const uint32_t* bits;      // [rows][K/32]
     int64_t words;             // K/32
     struct Raw { uint2 w; };
     __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
         Raw r;
-        r.w = ok ? ldg_u2_nc(bits + (int64_t)row * words + (int64_t)kc * 2) : make_uint2(0u, 0u);
+        r.w = ok ? ldg_u2_l1(bits + (int64_t)row * words + (int64_t)kc * 2) : make_uint2(0u, 0u);
         return r;
     }
     template <int P>
@@ -142,30 +164,51 @@ struct EpiArgs {
 };
 
 // ----------------------------------------------------------------- kernel ----
+// Persistent: CTA b walks tiles b, b + gridDim.x, ...; tile t = (n-tile, token
+// tile, K split) with the n-tile fastest, so CTAs running together share one
+// activation tile in L2.  The stage ring and the two accumulators run
+// continuously across tiles; the epilogue of a tile overlaps the MMAs of the
+// next.
+struct TileMap {
+    // a unit is `cl` weight tiles (one per CTA of a cluster) x one token tile
+    // x one K split; tiles_np = ceil(tiles_n / cl) units along the rows
+    int tiles_n, tiles_np, tiles_m, splits, total, nk_total;
+    __device__ __forceinline__ void decode(int t, int& np, int& m, int& z) const {
+        np = t % tiles_np;
+        const int rest = t / tiles_np;
+        m = rest % tiles_m;
+        z = rest / tiles_m;
+    }
+    __device__ __forceinline__ int kc0(int z) const { return (int)(((int64_t)nk_total * z) / splits); }
+    __device__ __forceinline__ int kc1(int z) const { return (int)(((int64_t)nk_total * (z + 1)) / splits); }
+};
+
 template <class Dec, int MODE>
 __global__ void __launch_bounds__(UM_THREADS, 1)
-umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const EpiArgs ep, int T, int R, int K,
-                 int BN, int tmem_cols) {
+umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const EpiArgs ep, int T, int R, int BN,
+                 int tmem_cols, const TileMap tm, int S, int NACC, int cl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_bytes = BN * 128;
-    UmmaBars* bars = reinterpret_cast<UmmaBars*>(smem + UM_STAGES * stage_bytes);
-
+    UmmaBars* bars = reinterpret_cast<UmmaBars*>(smem + S * stage_bytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * UM_BM;
-    const int m0 = blockIdx.y * BN;
-    const int nk_total = K / UM_BK;
-    const int kc0 = (int)(((int64_t)nk_total * blockIdx.z) / gridDim.z);
-    const int kc1 = (int)(((int64_t)nk_total * (blockIdx.z + 1)) / gridDim.z);
-    const int nk = kc1 - kc0;
+    // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
+    // tiles of the same unit and share its activation tile: each loads 1/cl
+    // of it with a multicast TMA into every CTA's ring.
+    const int rank = cl > 1 ? (int)cluster_ctarank() : 0;
+    const int unit0 = blockIdx.x / cl, units = gridDim.x / cl;
+    const uint16_t cmask = (uint16_t)((1u << cl) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < UM_STAGES; ++s) {
             mbar_init(&bars->full_b[s], 1);
             mbar_init(&bars->full_a[s], 4);
-            mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->empty[s], (uint32_t)cl);     // every cluster CTA's MMA must release it
         }
-        mbar_init(&bars->done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->acc_full[b], 1);
+            mbar_init(&bars->acc_empty[b], 4);
+        }
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&xmap);
@@ -176,108 +219,196 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     }
     tc_fence_before();
     __syncthreads();
+    if (cl > 1) cluster_sync();                          // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t a_col0 = (uint32_t)BN;
+    const uint32_t a_col0 = (uint32_t)(NACC * BN);
     volatile int* abort_flag = &bars->abort;
 
     pdl_launch_dependents();
 
     if (warp == 0) {
-        if (lane == 0) {                       // TMA producer (activation tiles)
+        if (lane == 0) {                                   // ---- TMA producer
             pdl_wait();
-            int issued = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % UM_STAGES;
-                const uint32_t ph = (uint32_t)(i / UM_STAGES) & 1u;
-                if (i >= UM_STAGES && !mbar_wait(&bars->empty[s], ph ^ 1u)) { *abort_flag = 1; break; }
-                if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bars->full_b[s], (uint32_t)stage_bytes);
-                tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full_b[s], (kc0 + i) * UM_BK, m0);
-                ++issued;
+            int it = 0;
+            bool ok = true;
+            for (int t = unit0; t < tm.total && ok; t += units) {
+                int np, m, z;
+                tm.decode(t, np, m, z);
+                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (uint32_t)(it / S) & 1u;
+                    if ((it >= S && !mbar_wait(&bars->empty[s], ph ^ 1u)) || *abort_flag) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->full_b[s], (uint32_t)stage_bytes);
+                    const int part = BN / cl;                  // token rows this CTA loads
+                    if (cl > 1)
+                        tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full_b[s], kc * UM_BK,
+                                       m * BN + rank * part, cmask);
+                    else
+                        tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full_b[s], kc * UM_BK, m * BN);
+                }
             }
-            if (*abort_flag) {                 // let copies already issued land before exit
-                for (int i = issued - UM_STAGES < 0 ? 0 : issued - UM_STAGES; i < issued; ++i)
-                    mbar_wait(&bars->full_b[i % UM_STAGES], (uint32_t)(i / UM_STAGES) & 1u);
-            }
+            // let the copies already issued land before the CTA can exit
+            for (int i = (it > S ? it - S : 0); i < it; ++i)
+                mbar_wait(&bars->full_b[i % S], (uint32_t)(i / S) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0) {                       // MMA issuer
+        if (lane == 0) {                                   // ---- MMA issuer
             const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % UM_STAGES;
-                const uint32_t ph = (uint32_t)(i / UM_STAGES) & 1u;
-                if (!mbar_wait(&bars->full_b[s], ph) || !mbar_wait(&bars->full_a[s], ph) || *abort_flag) {
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = unit0; t < tm.total && ok; t += units, ++lt) {
+                int np, m, z;
+                tm.decode(t, np, m, z);
+                const int buf = lt % NACC, use = lt / NACC;
+                if (use >= 1 && !mbar_wait(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
+                const uint32_t dcol = tmem + (uint32_t)(buf * BN);
+                const int k0 = tm.kc0(z), k1 = tm.kc1(z);
+                for (int kc = k0; kc < k1; ++kc, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (uint32_t)(it / S) & 1u;
+                    if (!mbar_wait(&bars->full_b[s], ph) || !mbar_wait(&bars->full_a[s], ph) || *abort_flag) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
 #pragma unroll
-                for (int j = 0; j < UM_BK / 16; ++j)
-                    umma_f16_ts(tmem, tmem + a_col0 + (uint32_t)(s * (UM_BK / 2) + j * 8), bdesc + (uint64_t)(2 * j),
-                                idesc, (i > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&bars->empty[s]);
+                    for (int j = 0; j < UM_BK / 16; ++j)
+                        umma_f16_ts(dcol, tmem + a_col0 + (uint32_t)(s * (UM_BK / 2) + j * 8),
+                                    bdesc + (uint64_t)(2 * j), idesc, (kc > k0 || j > 0) ? 1u : 0u);
+                    if (cl > 1) umma_commit_mc(&bars->empty[s], cmask);
+                    else umma_commit(&bars->empty[s]);
+                }
+                umma_commit(&bars->acc_full[buf]);
             }
-            umma_commit(&bars->done);
         }
-    } else if (warp >= 4) {
-        const int q = warp & 3;
-        const int row = n0 + q * 32 + lane;
-        const bool rok = row < R;
+    } else if (warp >= 4 && warp < 12) {                   // ---- decoders
+        // warp pair (q, h): lane quarter q, stages with item parity h
+        const int q = warp & 3, h = (warp - 4) >> 2;
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-
-        auto process = [&](int i, const typename Dec::Raw& raw) -> bool {
-            const int s = i % UM_STAGES;
-            const uint32_t ph = (uint32_t)(i / UM_STAGES) & 1u;
-            if (i >= UM_STAGES && !mbar_wait(&bars->empty[s], ph ^ 1u)) return false;
-            if (*abort_flag) return false;
-            tc_fence_after();
-            uint32_t v[32];
-            dec.decode(raw, v);
-            tmem_st_32x32b_x32(lane_addr + a_col0 + (uint32_t)(s * (UM_BK / 2)), v);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->full_a[s]);
-            return true;
+        constexpr int PF = 3;                              // own items prefetched ahead
+        // flattened walk over this CTA's (tile, kc) items, two cursors
+        struct Cur {
+            int t, kc, k1, row;
+            bool rok;
         };
-        auto ld = [&](int i) { return dec.load(rok ? row : 0, rok && i < nk, kc0 + (i < nk ? i : 0)); };
-
-        typename Dec::Raw r0 = ld(0), r1 = ld(1), r2 = ld(2), r3 = ld(3);
-        bool ok = true;
-        for (int i = 0; i < nk && ok; i += 4) {
-            ok = process(i, r0);
-            r0 = ld(i + 4);
-            if (ok && i + 1 < nk) { ok = process(i + 1, r1); r1 = ld(i + 5); }
-            if (ok && i + 2 < nk) { ok = process(i + 2, r2); r2 = ld(i + 6); }
-            if (ok && i + 3 < nk) { ok = process(i + 3, r3); r3 = ld(i + 7); }
+        auto start = [&](Cur& c, int t) {
+            c.t = t;
+            if (t < tm.total) {
+                int np, m, z;
+                tm.decode(t, np, m, z);
+                c.kc = tm.kc0(z);
+                c.k1 = tm.kc1(z);
+                c.row = (np * cl + rank) * UM_BM + q * 32 + lane;
+                c.rok = c.row < R;
+            }
+        };
+        auto step = [&](Cur& c) {
+            if (++c.kc >= c.k1) start(c, c.t + units);
+        };
+        Cur ld, pr;
+        start(ld, unit0);
+        start(pr, unit0);
+        int ld_it = 0;
+        typename Dec::Raw ring[PF];
+        // advance the load cursor to this warp's first item and prefetch PF items
+        auto next_own = [&](Cur& c, int& i) {
+            while (c.t < tm.total && (i & 1) != h) { step(c); ++i; }
+        };
+        next_own(ld, ld_it);
+#pragma unroll
+        for (int j = 0; j < PF; ++j) {
+            const bool live = ld.t < tm.total;
+            ring[j] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
+            if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
         }
-        if (!ok) *abort_flag = 1;
-
-        // ---------------- epilogue ----------------
-        if (mbar_wait(&bars->done, 0) && !*abort_flag) {
+        int it = 0, slot = 0;
+        bool ok = true;
+        while (pr.t < tm.total && ok) {
+            if ((it & 1) == h) {
+                const typename Dec::Raw cur = ring[0];
+#pragma unroll
+                for (int j = 0; j + 1 < PF; ++j) ring[j] = ring[j + 1];
+                {
+                    const bool live = ld.t < tm.total;
+                    ring[PF - 1] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
+                    if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
+                }
+                const int s = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
+                if ((it >= S && !mbar_wait(&bars->empty[s], ph ^ 1u)) || *abort_flag) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[32];
+                dec.decode(cur, v);
+                tmem_st_32x32b_x32(lane_addr + a_col0 + (uint32_t)(s * (UM_BK / 2)), v);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->full_a[s]);
+            }
+            step(pr);
+            ++it;
+            (void)slot;
+        }
+    } else if (warp >= 12) {                               // ---- epilogue
+        const int q = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        bool waited = false;
+        int lt = 0;
+        for (int t = unit0; t < tm.total; t += units, ++lt) {
+            int np, m, z;
+            tm.decode(t, np, m, z);
+            const int n = np * cl + rank;
+            const int buf = lt % NACC, use = lt / NACC;
+            if (!mbar_wait(&bars->acc_full[buf], (uint32_t)use & 1u) || *abort_flag) {
+                *abort_flag = 1;
+                break;
+            }
             tc_fence_after();
-            pdl_wait();
+            if (!waited) {
+                pdl_wait();
+                waited = true;
+            }
+            const int row = n * UM_BM + q * 32 + lane;
+            const bool rok = row < R;
+            const int m0 = m * BN;
+            const float vs = (rok && (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM)) ? ep.vec[row] : 1.f;
             float colacc = 0.f;
             for (int cc = 0; cc < BN; cc += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_addr + (uint32_t)cc, v);
+                tmem_ld_32x32b_x32(lane_addr + (uint32_t)(buf * BN + cc), v);
                 tmem_wait_ld();
+                if (cc + 32 >= BN) {                       // accumulator fully read: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->acc_empty[buf]);
+                }
                 if (!rok) continue;
-                const float vs = (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) ? ep.vec[row] : 1.f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int m = m0 + cc + i;
-                    if (m >= T) break;
+                const int nvalid = (T - (m0 + cc)) < 32 ? (T - (m0 + cc)) : 32;
+                const int64_t o0 = (int64_t)(m0 + cc) * ep.ldo + row;
+                auto one = [&](int i) {
                     const float a = __uint_as_float(v[i]);
-                    const int64_t o = (int64_t)m * ep.ldo + row;
+                    const int64_t o = o0 + (int64_t)i * ep.ldo;
                     if (MODE == EPI_STORE) {
                         ep.out[o] = a * ep.oscale;
                     } else if (MODE == EPI_ATOMIC) {
                         atomicAdd(ep.out + o, a * ep.oscale);
                     } else if (MODE == EPI_PARTIAL) {
-                        ep.out[(int64_t)blockIdx.z * T * ep.ldo + o] = a;
+                        ep.out[(int64_t)z * T * ep.ldo + o] = a;
                     } else {
                         const float w = a * ep.oscale;
                         if (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) {
@@ -286,15 +417,24 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                         }
                         if (MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) colacc = fmaf(w, ep.other[o], colacc);
                     }
+                };
+                if (nvalid == 32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) one(i);
+                } else {
+                    for (int i = 0; i < nvalid; ++i) one(i);
                 }
             }
             if ((MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) && rok)
-                ep.colpart[(int64_t)blockIdx.y * ep.ldo + row] = colacc;
+                ep.colpart[(int64_t)m * ep.ldo + row] = colacc;
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    // every MMA of this CTA has completed (the epilogue saw each tile), so its
+    // multicast commits have landed; wait for the peers' to land here too
+    if (cl > 1) cluster_sync();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)tmem_cols);
@@ -302,23 +442,61 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
 }
 
 // Host: launch one GEMM.  act16 is f16 [T][K] (row pitch K), staged in the
-// decoder's K order; R = plane rows; splits = K splits (gridDim.z).
+// decoder's K order; R = plane rows; splits = K splits.
 template <class Dec, int MODE>
 cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN, int splits,
                         cudaStream_t st) {
+    if (BN > UM_MAX_BN || BN % 32 != 0 || BN < 32) return cudaErrorInvalidValue;
+    const int tiles_n = (R + UM_BM - 1) / UM_BM;
+    const int cl = (tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
     CUtensorMap xmap;
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
-                            (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                            (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    // ring depth and accumulator count: two accumulators (epilogue overlaps
+    // the next tile) when they fit next to the A stages in 512 TMEM columns,
+    // else one; the B ring must also fit the shared memory.
+    int S, NACC;
+    if (2 * BN + 8 * (UM_BK / 2) <= 512) { S = 8; NACC = 2; }
+    else if (2 * BN + 4 * (UM_BK / 2) <= 512) { S = 4; NACC = 2; }
+    else { S = 6; NACC = 1; }
+    while (S > 2 && (size_t)S * BN * 128 + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
     int tmem_cols = 32;
-    while (tmem_cols < BN + UM_STAGES * (UM_BK / 2)) tmem_cols <<= 1;
-    const size_t smem = (size_t)UM_STAGES * BN * 128 + sizeof(UmmaBars) + 1024;
-    const dim3 grid((unsigned)((R + UM_BM - 1) / UM_BM), (unsigned)((T + BN - 1) / BN), (unsigned)splits);
+    while (tmem_cols < NACC * BN + S * (UM_BK / 2)) tmem_cols <<= 1;
+    // At least 120 KB of shared memory: no two CTAs of this kernel can share
+    // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
+    // (which a cluster barrier could otherwise turn into a deadlock).
+    size_t smem = (size_t)S * BN * 128 + 1024 + sizeof(UmmaBars) + 1024;
+    if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
+    TileMap tm;
+    tm.tiles_n = tiles_n;
+    tm.tiles_np = (tiles_n + cl - 1) / cl;
+    tm.tiles_m = (T + BN - 1) / BN;
+    tm.splits = splits;
+    tm.total = tm.tiles_np * tm.tiles_m * splits;
+    tm.nk_total = K / UM_BK;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int units = tm.total < sms / cl ? tm.total : sms / cl;
     cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(umma_gemm_kernel<Dec, MODE>, grid, dim3(UM_THREADS), smem, st, xmap, dec, ep, T, R, K, BN,
-                      tmem_cols);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * cl));
+    cfg.blockDim = dim3(UM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE>, xmap, dec, ep, T, R, BN, tmem_cols, tm, S, NACC, cl);
 }
 
 inline int umma_pick_bn(int T) {

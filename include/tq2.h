@@ -144,6 +144,23 @@ TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64
                          int path, void* stream);
 
 /*
+ * tq2_gemm_grouped -- G independent decode-shape GEMMs in one launch:
+ * out_g[m,n] = sum_k x_g[m,k] * W_g[n,k] for g < G, each as tq2_gemm with
+ * M <= 2 computes it (same kernel, same per-output arithmetic, so results
+ * are bit-identical to G separate tq2_gemm calls).  One launch streams all
+ * G weights, so independent projections that read the same activations
+ * (or different ones) do not pay G kernel launches and G dependency waits.
+ *
+ *   hs      HOST array of G handles; all must have the same K.
+ *   xs      HOST array of G DEVICE pointers, float[M][K] each, 16-byte aligned.
+ *   outs    HOST array of G DEVICE pointers, float[M][N_g] each (overwritten).
+ *   G       1..64;  M in {1, 2};  K the handles' K.  Else TQ2_ESHAPE.
+ *   stream  asynchronous; no scratch is allocated.
+ */
+TQ2_API tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float* const* outs, int G,
+                                    int64_t M, int64_t K, void* stream);
+
+/*
  * tq2_unpack -- rebuild the AoS bytes from the device planes (round trip of
  * tq2_upload).  aos_out: HOST buffer of N*(K/128)*34 bytes.  Synchronous.
  */

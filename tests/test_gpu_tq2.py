@@ -100,6 +100,32 @@ def test_gemv_large_k_chunks(lib):
         assert np.all(np.abs(got - ref) <= (2.0 ** -10) * absref + 1e-7)
 
 
+def test_gemv_grouped_matches_single_calls(lib):
+    import torch
+    K = 2048
+    shapes = [(4096, 11), (40, 12), (17, 13), (1000, 14)]
+    ws, auos = [], []
+    for N, key in shapes:
+        a = synth.random_tq2(N, K, key)
+        auos.append(a)
+        ws.append(lib.tq2_upload(a, N, K))
+    for M in (1, 2):
+        xs = [to_dev(synth.random_x(M, K, 50 + g)) for g in range(len(ws))]
+        outs = [torch.full((M, w.N), float("nan"), device="cuda") for w in ws]
+        lib.tq2_gemm_grouped(ws, xs, outs)
+        lib.device_status()
+        for g, w in enumerate(ws):
+            single = torch.empty_like(outs[g])
+            lib.tq2_gemm(w, xs[g], single)
+            lib.device_status()
+            assert torch.equal(outs[g], single), (M, g)
+            ref, absref, _, _ = oracle_gemm(auos[g], w.N, K, xs[g].cpu().numpy())
+            check_skinny(outs[g].cpu().numpy().astype(np.float64), ref, absref, f"grouped M={M} g={g}")
+    with pytest.raises(lib.TQ2Error):                       # M = 3 is not a grouped shape
+        x3 = [torch.zeros((3, K), device="cuda") for _ in ws]
+        lib.tq2_gemm_grouped(ws, x3, [torch.zeros((3, w.N), device="cuda") for w in ws])
+
+
 def test_gemv_full_size(lib):
     cfg = synth.GEMV
     N, K = cfg["N"], cfg["K"]
