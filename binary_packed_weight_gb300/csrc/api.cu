@@ -72,6 +72,18 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dtype, 3, base, d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tq2
 
 extern "C" {
@@ -97,7 +109,7 @@ tq2_status tq2_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq2_device_status: stream");
     const unsigned int err = tq2::read_clear_dev_error_skinny(S(stream)) | tq2::read_clear_dev_error_umma(S(stream)) |
-                             tq2::read_clear_dev_error_blr(S(stream));
+                             tq2::read_clear_dev_error_blr(S(stream)) | tq2::read_clear_dev_error_gemv(S(stream));
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tq2_device_status");
     if (err) return fail(TQ2_ETIMEOUT, "a bounded device-side wait ran out (record 0x%x)", err);
@@ -118,8 +130,12 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     w->N = N;
     w->K = K;
     cudaGetDevice(&w->device);
-    cudaError_t e = cudaMalloc(&w->codes, (size_t)(N * K / 4));
-    if (e == cudaSuccess) e = cudaMalloc(&w->scales, (size_t)nblocks * 2);
+    // Both planes carry a little zeroed padding: the GEMV's TMA box may run up
+    // to 128 bytes past the last row's codes, its scale copy up to 14 bytes.
+    cudaError_t e = cudaMalloc(&w->codes, (size_t)(N * K / 4) + 128);
+    if (e == cudaSuccess) e = cudaMemset(w->codes + N * K / 4, 0, 128);
+    if (e == cudaSuccess) e = cudaMalloc(&w->scales, (size_t)nblocks * 2 + 16);
+    if (e == cudaSuccess) e = cudaMemset(w->scales + nblocks, 0, 16);
     if (e != cudaSuccess) {
         cudaFree(w->codes);
         delete w;
@@ -136,6 +152,12 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
         cudaFree(w->scales);
         delete w;
         return cuda_fail(e, "tq2_upload");
+    }
+    if (!tq2::make_gemv_maps(w)) {
+        cudaFree(w->codes);
+        cudaFree(w->scales);
+        delete w;
+        return fail(TQ2_EUNSUPPORTED, "tq2_upload: cuTensorMapEncodeTiled refused the code-plane map");
     }
     *out = w;
     return TQ2_OK;
@@ -172,8 +194,8 @@ tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64_t M, in
     cudaStream_t st = S(stream);
     if (path == TQ2_PATH_SKINNY) {
         if (M > 16) return fail(TQ2_ESHAPE, "tq2_gemm: skinny kernel needs M <= 16");
-        if (M <= tq2::GEMV_MAX_M) {          // fused single-kernel GEMV, no scratch
-            cudaError_t e = tq2::launch_gemv(h->codes, h->scales, x, out, (int)M, (int)N, (int)K, st);
+        if (tq2::gemv_supports((int)M, K)) {   // fused single-kernel GEMV, no scratch
+            cudaError_t e = tq2::launch_gemv(&h, &x, &out, 1, (int)M, st);
             if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm: gemv launch");
             return TQ2_OK;
         }
@@ -208,21 +230,19 @@ tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float*
                             int64_t K, void* stream) {
     if (!hs || !xs || !outs) return fail(TQ2_EINVAL, "tq2_gemm_grouped: null array");
     if (G < 1 || G > tq2::GEMV_MAX_JOBS) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= G <= %d", tq2::GEMV_MAX_JOBS);
-    if (M < 1 || M > tq2::GEMV_MAX_M) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= M <= %d", tq2::GEMV_MAX_M);
-    tq2::GemvTable tab;
-    tab.njobs = G;
-    tab.K = (int)K;
-    int64_t ctas = 0;
+    if (!tq2::gemv_supports((int)M, K))
+        return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= M <= %d and M*K <= %lld (M=%lld K=%lld)", tq2::GEMV_MAX_M,
+                    (long long)tq2::GEMV_MAX_MK, (long long)M, (long long)K);
+    int64_t rows = 0;
     for (int g = 0; g < G; ++g) {
         const tq2_handle h = hs[g];
         if (!h || !xs[g] || !outs[g]) return fail(TQ2_EINVAL, "tq2_gemm_grouped: null entry %d", g);
         if (h->K != K) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: entry %d has K=%lld, not %lld", g, (long long)h->K, (long long)K);
         if ((reinterpret_cast<uintptr_t>(xs[g]) & 15) != 0) return fail(TQ2_EINVAL, "tq2_gemm_grouped: x %d not 16-byte aligned", g);
-        tab.job[g] = tq2::GemvJob{h->codes, h->scales, xs[g], outs[g], (int)h->N, (int)ctas};
-        ctas += (h->N + 15) / 16;
+        rows += h->N;
     }
-    if (ctas >= ((int64_t)1 << 31)) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: too many rows");
-    cudaError_t e = tq2::launch_gemv_table(tab, (int)M, S(stream));
+    if (rows >= ((int64_t)1 << 31)) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: too many rows");
+    cudaError_t e = tq2::launch_gemv(hs, xs, outs, G, (int)M, S(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm_grouped");
     return TQ2_OK;
 }

@@ -3,18 +3,37 @@
 //   out[m,n] = sum_k x[m,k] * W[n,k],  W[n,k] = (c-1)*d   (BlockTQ2_0_g128,
 //   "oxibonsai-kernels 0.2.1, src/gpu_backend/metal_graph/tests_gemm_tq2.rs")
 //
-// One kernel per GEMV (no staging kernel, no scratch):
-//   * A CTA owns 16 weight rows (one m16 fragment); its 8 warps split K.
-//   * Before griddepcontrol.wait each lane loads the packed codes and scales
-//     of its rows for its first K chunk: the weights never depend on earlier
-//     work, so they stream in while the previous kernel on the stream drains.
-//   * After the wait each warp converts the x values of its own K chunk to
-//     the hi/lo f16 B fragments of mma.m16n8k16 (shared memory, warp-private)
-//     together with the per-block correction sum_k (m_q + 1) x_k.
-//   * Codes are decoded with decode_word_offset (shift + mask|magic, no
-//     subtraction): the MMA accumulates (m_q + c) x per 128-block in f32; the
-//     block result is d * (acc_hi + acc_lo - correction).
-//   * The warps' partial sums meet in shared memory in a fixed order.
+// One kernel per launch (one GEMV, or up to 64 independent GEMVs sharing K and
+// M), no scratch.  A CTA is one producer warp and eight consumer warps; it
+// owns a contiguous range of work units.
+//
+//   * The producer streams the weights.  A stage is 16 KB of codes fetched by
+//     ONE TMA load through a 3D view of the code plane -- (128-byte piece,
+//     row, piece index) -- with 128-byte swizzling, so each warp's share
+//     lands as [16 rows][128 B] (4 blocks of 128 k per row) and the MMA
+//     fragments read back without bank conflicts.  Per unit one
+//     cp.async.bulk brings the unit's block scales (consecutive rows' scales
+//     are contiguous in the scale plane) into a ring of slots.  The weights
+//     never depend on earlier work on the stream, so this starts at once.
+//   * The consumers wait for the previous kernel (griddepcontrol.wait),
+//     convert x once into the hi/lo f16 B fragments of mma.m16n8k16 in
+//     shared memory, then per stage decode their 4 blocks (shift +
+//     mask|magic, see gv_pair) and issue the MMAs: one accumulator chain
+//     per block, four interleaved per warp, f32 accumulate, block scale
+//     applied to the block result d * (acc - correction).
+//   * Two ways to cut the work (the smem addressing of a warp's share is the
+//     same in both):
+//       k-split (small N): a unit is 16 rows; a stage covers them over 32
+//         blocks, warp w taking blocks 4w..4w+3; the warps' sums meet in
+//         shared memory and are added in a fixed order.
+//       row-split (N large enough to fill the GPU): a unit is 128 rows; a
+//         stage covers them over 4 blocks, warp w taking rows 16w..16w+15
+//         over all of K, so no cross-warp reduction is needed.  Each warp
+//         keeps eight partial sums that mirror the k-split warps, so both
+//         ways give bit-identical results.
+// With few units per CTA, shared memory stays under ~110 KB so the next
+// kernel on the stream (launched early through programmatic dependent
+// launch) fits beside this one on every SM and streams its own weights.
 #include "ptx.cuh"
 #include "tq2_internal.h"
 
@@ -22,14 +41,45 @@ namespace tq2 {
 
 namespace {
 
-constexpr int GV_WARPS = 8;
-constexpr int GV_CHUNK = 4;            // 128-blocks per warp per chunk
+constexpr int GV_CONS = 8;                         // consumer warps
+constexpr int GV_THREADS = (GV_CONS + 1) * 32;     // + one producer warp
+constexpr int GV_BPW = 4;                          // 128-blocks per consumer warp per stage
+constexpr int GV_PIECE = 128;                      // bytes of one row's codes for 4 blocks
+constexpr int GV_WARP_BYTES = 16 * GV_PIECE;       // a warp's share of a stage: 16 rows x 128 B
+constexpr int GV_STAGE = GV_CONS * GV_WARP_BYTES;  // 16 KB
+constexpr int GV_MAX_STAGES = 16;
+constexpr int GV_MAX_SSLOTS = 8;                   // scale slots (one unit each)
+constexpr int GV_SMEM_PAIR = 110 * 1024;           // two CTAs per SM (with the static job table)
+constexpr int GV_SMEM_MAX = 225 * 1024;            // dynamic part; + up to 2 KB static job table
 
-__device__ __forceinline__ uint2 ldg_nc_u2(const uint8_t* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
+enum GvMode { GV_KSPLIT = 0, GV_ROWS = 1 };
+__host__ __device__ constexpr int gv_unit_rows(int mode) { return mode == GV_ROWS ? 16 * GV_CONS : 16; }
+__host__ __device__ constexpr int gv_stage_blocks(int mode) { return mode == GV_ROWS ? GV_BPW : GV_BPW * GV_CONS; }
+
+struct GemvJob {
+    CUtensorMap map;              // the weight's code-plane map for the launch's mode
+    const uint16_t* scales;
+    const float* x;
+    float* out;
+    int N;
+    int unit0;                    // first unit of this job in the launch
+};
+template <int NJ>
+struct GemvTab {
+    GemvJob job[NJ];
+    int njobs;
+    int K;
+};
+
+// The per-job fields the loops read, copied to shared memory once: the job
+// table is a kernel parameter, and reading it with a runtime index goes
+// through the constant cache.
+struct GvJobS {
+    const uint16_t* scales;
+    const float* x;
+    float* out;
+    int N, unit0;
+};
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);      // .x (low 16 bits) = lo
@@ -44,184 +94,471 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_
     lo = pack_h2(v0 - back.x, v1 - back.y);
 }
 
+// Pair q of a 16-code word (elements q and q+8 at bits 2q and 16+2q) as the
+// exact f16 pair (m_q + c_lo, m_q + c_hi): the code is brought to bit
+// P in {4, 6, 8} of each half by one of two shifts (or none) and OR-ed into
+// the mantissa of m_q = 2^(10-P).
+//   q:    0   1   2   3   4   5   6   7
+//   word: <<4 <<4  .   .   .  >>6 >>6 >>6
+//   P:    4   6   4   6   8   4   6   8
+//   m_q:  64  16  64  16  4   64  16  4
 template <int Q>
-__device__ __forceinline__ uint32_t opair(uint32_t w) {
+__device__ __forceinline__ uint32_t gv_pair(uint32_t w) {
     if constexpr (Q == 0) return offset_pair<4>(w << 4);
     else if constexpr (Q == 1) return offset_pair<6>(w << 4);
-    else if constexpr (Q == 2) return offset_pair<8>(w << 4);
-    else if constexpr (Q == 3) return offset_pair<4>(w >> 2);
-    else if constexpr (Q == 4) return offset_pair<6>(w >> 2);
-    else if constexpr (Q == 5) return offset_pair<8>(w >> 2);
-    else if constexpr (Q == 6) return offset_pair<4>(w >> 8);
-    else return offset_pair<6>(w >> 8);
+    else if constexpr (Q == 2) return offset_pair<4>(w);
+    else if constexpr (Q == 3) return offset_pair<6>(w);
+    else if constexpr (Q == 4) return offset_pair<8>(w);
+    else if constexpr (Q == 5) return offset_pair<4>(w >> 6);
+    else if constexpr (Q == 6) return offset_pair<6>(w >> 6);
+    else return offset_pair<8>(w >> 6);
+}
+// m_q + 1 for the element at position e (0..15) of a word.
+__host__ __device__ constexpr float gv_plus_one(int e) {
+    return (e % 8 == 4 || e % 8 == 7) ? 5.f : ((e % 8 == 1 || e % 8 == 3 || e % 8 == 6) ? 17.f : 65.f);
+}
+
+// The A fragment of k16 step j (0..3) of a word: rows g and g+8 from words
+// wa and wb; positions 2t,2t+1 hold pair 2j, positions 2t+8,2t+9 pair 2j+1.
+template <int J>
+__device__ __forceinline__ void gv_afrag(uint32_t wa, uint32_t wb, uint32_t (&a)[4]) {
+    a[0] = gv_pair<2 * J>(wa);
+    a[1] = gv_pair<2 * J>(wb);
+    a[2] = gv_pair<2 * J + 1>(wa);
+    a[3] = gv_pair<2 * J + 1>(wb);
+}
+
+struct GvLayout {
+    int nb, nch;
+    uint32_t off_red, off_corr, off_sc, sc_bytes, off_xs, off_ring, total;
+};
+
+// Shared-memory carve (byte offsets from the dynamic base; barriers first).
+__host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stages, int sslots) {
+    GvLayout L;
+    L.nb = K / 128;
+    L.nch = (L.nb + gv_stage_blocks(mode) - 1) / gv_stage_blocks(mode);
+    L.off_red = 512;                                                   // full, empty, sfull, sempty
+    L.off_corr = L.off_red + (mode == GV_KSPLIT ? 2u * GV_CONS * 16 * MT * 4 : 0u);
+    L.off_sc = L.off_corr + (((uint32_t)L.nb + 3u) & ~3u) * MT * 4;             // whole pieces (float4 reads)
+    L.sc_bytes = ((uint32_t)gv_unit_rows(mode) * L.nb * 2 + 16u + 15u) & ~15u;
+    L.off_xs = L.off_sc + (uint32_t)sslots * L.sc_bytes;
+    L.off_ring = L.off_xs + (uint32_t)L.nb * 8 * (2 * MT) * 4 * 8;              // [nb][2MT][4][8] uint2
+    L.total = L.off_ring + 1024u + (uint32_t)stages * GV_STAGE;                  // + room to align to 1 KB
+    return L;
+}
+
+// One warp's share of a stage: 4 consecutive blocks blk0.. of rows g and g+8
+// (nv of them valid).  pc points at the warp's 2 KB region + g*128 + 8*(t&1);
+// 16-byte chunk (2i + t/2) of a 128-byte row is stored at chunk
+// (2i + t/2) ^ (row & 7), and row g+8 sits 1 KB after row g.  scA points at
+// row g's scales (row g+8's are 8*nb further).  x fragments are stored
+// [block][column][t][k16 step] (uint2), so one 16-byte load serves two
+// steps; each block's eight MMAs form one accumulator chain, the four
+// blocks' chains interleave.
+template <int MT>
+__device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const uint2* xs, const float* corr,
+                                         int blk0, int nv, int nb, const uint16_t* scA, int tm, float& totA,
+                                         float& totB) {
+    uint2 ca[GV_BPW], cb[GV_BPW];
+    const uint4* xb[GV_BPW];
+#pragma unroll
+    for (int i = 0; i < GV_BPW; ++i) {
+        const uint8_t* p = pc + ((((2 * i + (t >> 1)) ^ g) & 7) << 4);
+        ca[i] = *reinterpret_cast<const uint2*>(p);
+        cb[i] = *reinterpret_cast<const uint2*>(p + 8 * GV_PIECE);
+        xb[i] = reinterpret_cast<const uint4*>(xs + ((min(blk0 + i, nb - 1) * (2 * MT) + g) * 4 + t) * 8);
+    }
+    float acc[GV_BPW][4];
+#pragma unroll
+    for (int i = 0; i < GV_BPW; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
+    const bool bl = g < 2 * MT;
+    // steps 0-3 decode word x (k 32t..32t+15 of the block), 4-7 word y
+#define GV_STEP2(S)                                                                         \
+    _Pragma("unroll") for (int i = 0; i < GV_BPW; ++i) {                                    \
+        const uint4 b = bl ? xb[i][(S) / 2] : make_uint4(0u, 0u, 0u, 0u);                   \
+        const uint32_t w0 = (S) < 4 ? ca[i].x : ca[i].y, w1 = (S) < 4 ? cb[i].x : cb[i].y;   \
+        uint32_t a[4];                                                                      \
+        gv_afrag<(S) % 4>(w0, w1, a);                                                       \
+        mma_16816_pure(acc[i], a, b.x, b.y);                                                \
+        gv_afrag<((S) + 1) % 4>(w0, w1, a);                                                 \
+        mma_16816_pure(acc[i], a, b.z, b.w);                                                \
+    }
+    GV_STEP2(0)
+    GV_STEP2(2)
+    GV_STEP2(4)
+    GV_STEP2(6)
+#undef GV_STEP2
+    // block scales (f16) and corrections of the four blocks
+    float dA[GV_BPW], dB[GV_BPW], cr[GV_BPW];
+    if ((nb & 3) == 0) {
+        const uint2 ua = *reinterpret_cast<const uint2*>(scA + blk0);
+        const uint2 ub = *reinterpret_cast<const uint2*>(scA + 8 * nb + blk0);
+        const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&ua.x));
+        const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&ua.y));
+        const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&ub.x));
+        const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&ub.y));
+        dA[0] = a01.x; dA[1] = a01.y; dA[2] = a23.x; dA[3] = a23.y;
+        dB[0] = b01.x; dB[1] = b01.y; dB[2] = b23.x; dB[3] = b23.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < GV_BPW; ++i) {
+            dA[i] = __half2float(__ushort_as_half(scA[blk0 + i]));
+            dB[i] = __half2float(__ushort_as_half(scA[8 * nb + blk0 + i]));
+        }
+    }
+    {
+        const float4* c4 = reinterpret_cast<const float4*>(corr + blk0 * MT);
+        float cv[GV_BPW * MT];
+#pragma unroll
+        for (int q = 0; q < MT; ++q) {
+            const float4 v = c4[q];
+            cv[4 * q] = v.x; cv[4 * q + 1] = v.y; cv[4 * q + 2] = v.z; cv[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < GV_BPW; ++i) cr[i] = (MT == 1 || tm == 0) ? cv[i * MT] : cv[i * MT + MT - 1];
+    }
+#pragma unroll
+    for (int i = 0; i < GV_BPW; ++i) {
+        if (i < nv) {
+            totA = fmaf(dA[i], (acc[i][0] + acc[i][1]) - cr[i], totA);
+            totB = fmaf(dB[i], (acc[i][2] + acc[i][3]) - cr[i], totB);
+        }
+    }
 }
 
 }  // namespace
 
-// Shared memory per warp: xs[blk][step][col][t] (uint2 B fragments, col =
-// 2*m + part) and corr[blk][m].
-template <int MT>
-struct GemvSmem {
-    uint2 xs[GV_WARPS][GV_CHUNK][8][2 * MT][4];
-    float corr[GV_WARPS][GV_CHUNK][MT];
-    float red[GV_WARPS][16][MT];
-};
+// 112 registers: two CTAs of 288 threads fill the register file exactly.
+template <int MT, int MODE, int NJ>
+__global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab<NJ> tab, int units, int stages,
+                                                 int sslots) {
+    constexpr int UR = gv_unit_rows(MODE);
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ GvJobS sj[NJ];
+    const GvLayout L = gv_layout(tab.K, MT, MODE, stages, sslots);
+    const int njobs = tab.njobs;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + GV_MAX_STAGES;
+    uint64_t* sfull = empty + GV_MAX_STAGES;
+    uint64_t* sempty = sfull + GV_MAX_SSLOTS;
+    float* red = reinterpret_cast<float*>(smem + L.off_red);       // [2][GV_CONS][16][MT] (k-split)
+    float* corr = reinterpret_cast<float*>(smem + L.off_corr);     // [nb][MT]
+    uint8_t* scb = smem + L.off_sc;                                // [sslots] x ([UR][nb] f16)
+    uint2* xs = reinterpret_cast<uint2*>(smem + L.off_xs);         // [nb][2MT][4][8]
+    // [stages][8 warps][16 rows][128 B], 1 KB aligned for the 128-byte swizzle
+    uint8_t* ring = smem + L.off_ring + ((1024u - ((smem_u32(smem) + L.off_ring) & 1023u)) & 1023u);
 
-template <int MT>
-__global__ void __launch_bounds__(GV_WARPS * 32) tq2_gemv_kernel(const __grid_constant__ GemvTable tab) {
-    __shared__ GemvSmem<MT> sm;
-    // the job this CTA belongs to (jobs are laid out back to back in blockIdx.x)
-    int job = 0;
-    while (job + 1 < tab.njobs && (int)blockIdx.x >= tab.job[job + 1].cta0) ++job;
-    const uint8_t* __restrict__ codes = tab.job[job].codes;
-    const uint16_t* __restrict__ scales = tab.job[job].scales;
-    const float* __restrict__ x = tab.job[job].x;
-    float* __restrict__ out = tab.job[job].out;
-    const int N = tab.job[job].N, K = tab.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int n0 = ((int)blockIdx.x - tab.job[job].cta0) * 16;
-    const int nb = K >> 7;
-    const int kb_begin = (nb * warp) / GV_WARPS, kb_end = (nb * (warp + 1)) / GV_WARPS;
-    const int rowA = n0 + g, rowB = n0 + g + 8;
-    const bool okA = rowA < N, okB = rowB < N;
-    const int64_t pitch = K >> 2;
-    const uint8_t* pA = codes + (int64_t)(okA ? rowA : 0) * pitch + 8 * t;
-    const uint8_t* pB = codes + (int64_t)(okB ? rowB : 0) * pitch + 8 * t;
-    const uint16_t* sA = scales + (int64_t)(okA ? rowA : 0) * nb;
-    const uint16_t* sB = scales + (int64_t)(okB ? rowB : 0) * nb;
+    const int nb = L.nb, nch = L.nch, K = tab.K;
+    const int u_begin = (int)(((int64_t)blockIdx.x * units) / gridDim.x);
+    const int u_end = (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x);
 
-    // staging role of this lane: word (blk = lane/8, tq = (lane/2)%4, w = lane%2)
-    const int st_blk = lane >> 3, st_t = (lane >> 1) & 3, st_w = lane & 1;
-
-    float totA[MT], totB[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) totA[m] = totB[m] = 0.f;
-
-    uint2 cA[GV_CHUNK], cB[GV_CHUNK];
-    float dA[GV_CHUNK], dB[GV_CHUNK];
-    auto load_chunk = [&](int kb0) {
-#pragma unroll
-        for (int c = 0; c < GV_CHUNK; ++c) {
-            const int kb = kb0 + c;
-            const bool v = kb < kb_end;
-            cA[c] = (v && okA) ? ldg_nc_u2(pA + kb * 32) : make_uint2(0u, 0u);
-            cB[c] = (v && okB) ? ldg_nc_u2(pB + kb * 32) : make_uint2(0u, 0u);
-            dA[c] = (v && okA) ? __half2float(__ushort_as_half(__ldg(sA + kb))) : 0.f;
-            dB[c] = (v && okB) ? __half2float(__ushort_as_half(__ldg(sB + kb))) : 0.f;
+    if ((int)threadIdx.x < njobs) {
+        const GemvJob& J = tab.job[threadIdx.x];
+        sj[threadIdx.x] = GvJobS{J.scales, J.x, J.out, J.N, J.unit0};
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], GV_CONS);
         }
-    };
-    load_chunk(kb_begin);
-    pdl_wait();
+        for (int s = 0; s < sslots; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sempty[s], GV_CONS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Dependents may launch now: they take SM room only where this grid
+    // leaves some, and their producers stream while this grid computes.
+    pdl_launch_dependents();
 
-#pragma unroll 1
-    for (int kb0 = kb_begin; kb0 < kb_end; kb0 += GV_CHUNK) {
-        // ---- stage this warp's x chunk: one 16-element word per lane and token
-        {
-            const int kb = kb0 + st_blk;
-            const bool live = kb < kb_end;              // uniform within each 8-lane group
-            const int k0 = (live ? kb : kb0) * 128 + 32 * st_t + 16 * st_w;
+    // unit -> (job, first row); a CTA's units are consecutive, so the job
+    // index only moves forward
+    auto locate = [&](int u, int& job, int& n0) {
+        while (job + 1 < njobs && u >= sj[job + 1].unit0) ++job;
+        n0 = (u - sj[job].unit0) * UR;
+    };
+
+    if (warp == GV_CONS) {
+        // ------------------------------------------------ producer warp ----
+        if (lane != 0) return;
+        int it = 0, job = 0;
+        bool ok = true;
+        for (int u = u_begin, ui = 0; u < u_end && ok; ++u, ++ui) {
+            int n0;
+            locate(u, job, n0);
+            const GvJobS& J = sj[job];
+            const int rows = min(UR, J.N - n0);
+            const int slot = ui % sslots;
+            if (ui >= sslots) ok = mbar_wait(&sempty[slot], ((ui / sslots) - 1) & 1);
+            if (!ok) break;
+            // rounded up to 16 bytes: the scale plane carries 16 bytes of padding
+            const uint32_t sbytes = ((uint32_t)rows * nb * 2 + 15u) & ~15u;
+            mbar_arrive_expect_tx(&sfull[slot], sbytes);
+            bulk_load(scb + slot * L.sc_bytes, J.scales + (int64_t)n0 * nb, sbytes, &sfull[slot]);
+            for (int c = 0; c < nch; ++c, ++it) {
+                const int s = it % stages;
+                if (it >= stages) ok = mbar_wait(&empty[s], ((it / stages) - 1) & 1);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)GV_STAGE);
+                tma_load_3d(ring + s * GV_STAGE, &tab.job[job].map, &full[s], 0, n0,
+                            MODE == GV_ROWS ? c : c * GV_CONS);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps ----
+    const int g = lane >> 2, t = lane & 3;
+    const int tm = t < MT ? t : MT - 1;          // token of this lane's D columns 2t, 2t+1 (if t < MT)
+    // staging role of this lane: block (lane / 8) of the pass, word pair t, half y
+    const int st_q = lane >> 3, st_t = (lane >> 1) & 3, st_y = lane & 1;
+    // x blocks this warp converts: k-split -- the ones it uses,
+    // c * 32 + 4 * warp + i, listed c-major; row-split -- warp, warp + 8, ...
+    int nbw = 0;
+    if (MODE == GV_KSPLIT) {
+#pragma unroll
+        for (int i = 0; i < GV_BPW; ++i) {
+            const int r = nb - GV_BPW * warp - i;
+            nbw += r > 0 ? (r + GV_BPW * GV_CONS - 1) / (GV_BPW * GV_CONS) : 0;
+        }
+    } else {
+        nbw = nb > warp ? (nb - warp + GV_CONS - 1) / GV_CONS : 0;
+    }
+    auto consumers_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(GV_CONS * 32) : "memory"); };
+
+    pdl_wait();
+    const float* staged = nullptr;
+    auto stage_x = [&](const float* x) {
+        if (MODE == GV_ROWS && staged) consumers_sync();     // everyone is done with the old x
+        for (int p = 0; p < (nbw + 3) / 4; ++p) {
+            const int li = 4 * p + st_q;                      // index in this warp's block list
+            const bool live = li < nbw;                       // uniform within each 8-lane group
+            const int blk = MODE == GV_KSPLIT ? (li / GV_BPW) * (GV_BPW * GV_CONS) + GV_BPW * warp + li % GV_BPW
+                                              : warp + GV_CONS * li;
+            const int k0 = (live ? blk : 0) * 128 + 32 * st_t + 16 * st_y;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 float e[16];
-                if (live) {
-                    const float4* src = reinterpret_cast<const float4*>(x + (int64_t)m * K + k0);
-                    const float4 q0 = __ldg(src), q1 = __ldg(src + 1), q2 = __ldg(src + 2), q3 = __ldg(src + 3);
-                    e[0] = q0.x; e[1] = q0.y; e[2] = q0.z; e[3] = q0.w; e[4] = q1.x; e[5] = q1.y;
-                    e[6] = q1.z; e[7] = q1.w; e[8] = q2.x; e[9] = q2.y; e[10] = q2.z; e[11] = q2.w;
-                    e[12] = q3.x; e[13] = q3.y; e[14] = q3.z; e[15] = q3.w;
-                } else {
+                const float4* src = reinterpret_cast<const float4*>(x + (int64_t)m * K + k0);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) e[i] = 0.f;
+                for (int v = 0; v < 4; ++v) {
+                    const float4 q = live ? __ldg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    e[4 * v] = q.x; e[4 * v + 1] = q.y; e[4 * v + 2] = q.z; e[4 * v + 3] = q.w;
                 }
                 float cs = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) cs = fmaf(offset_plus_one(i), e[i], cs);
+                for (int i = 0; i < 16; ++i) cs = fmaf(gv_plus_one(i), e[i], cs);
                 if (live) {
 #pragma unroll
-                    for (int sl = 0; sl < 4; ++sl) {         // k16 step 4*w + sl: pairs q = 2sl, 2sl+1
+                    for (int j = 0; j < 4; ++j) {               // k16 step 4y + j: pairs 2j, 2j+1
                         uint32_t h01, l01, h23, l23;
-                        split2(e[2 * sl], e[2 * sl + 8], h01, l01);
-                        split2(e[2 * sl + 1], e[2 * sl + 9], h23, l23);
-                        const int s = 4 * st_w + sl;
-                        sm.xs[warp][st_blk][s][2 * m][st_t] = make_uint2(h01, h23);
-                        sm.xs[warp][st_blk][s][2 * m + 1][st_t] = make_uint2(l01, l23);
+                        split2(e[2 * j], e[2 * j + 8], h01, l01);
+                        split2(e[2 * j + 1], e[2 * j + 9], h23, l23);
+                        uint2* d = xs + ((blk * (2 * MT) + 2 * m) * 4 + st_t) * 8 + 4 * st_y + j;
+                        d[0] = make_uint2(h01, h23);              // column 2m: hi
+                        d[32] = make_uint2(l01, l23);             // column 2m+1: lo
                     }
                 }
                 cs += __shfl_xor_sync(0xffffffffu, cs, 1);
                 cs += __shfl_xor_sync(0xffffffffu, cs, 2);
                 cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-                if (live && (lane & 7) == 0) sm.corr[warp][st_blk][m] = cs;
+                if (live && (lane & 7) == 0) corr[blk * MT + m] = cs;
             }
-            __syncwarp();
         }
-        // ---- decode + MMA per block
+        if (MODE == GV_ROWS) consumers_sync();                // every block converted
+        else __syncwarp();
+        staged = x;
+    };
+
+    int it = 0, job = 0;
+    bool dead = false;                            // a bounded wait ran out: skip the rest
+    const int rbase = MODE == GV_ROWS ? 16 * warp : 0;
+    for (int u = u_begin, ui = 0; u < u_end; ++u, ++ui) {
+        int n0;
+        locate(u, job, n0);
+        const GvJobS& J = sj[job];
+        if (J.x != staged) stage_x(J.x);
+        const int slot = ui % sslots;
+        if (!dead && !mbar_wait(&sfull[slot], (ui / sslots) & 1)) dead = true;
+        const uint16_t* scA = reinterpret_cast<const uint16_t*>(scb + slot * L.sc_bytes) + (rbase + g) * nb;
+        auto do_stage = [&](int c, float& ta, float& tb) {
+            const int s = it % stages;
+            if (!dead && !mbar_wait(&full[s], (it / stages) & 1)) dead = true;
+            const uint8_t* pc = ring + s * GV_STAGE + warp * GV_WARP_BYTES + g * GV_PIECE + 8 * (t & 1);
+            const int blk0 = MODE == GV_ROWS ? GV_BPW * c : c * (GV_BPW * GV_CONS) + GV_BPW * warp;
+            const int nv = min(GV_BPW, nb - blk0);              // valid blocks (warp-uniform)
+            if (!dead && nv > 0) gv_piece<MT>(pc, g, t, xs, corr, blk0, nv, nb, scA, tm, ta, tb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++it;
+        };
+        float totA = 0.f, totB = 0.f;            // rows rbase+g and rbase+g+8, token tm
+        if (MODE == GV_KSPLIT) {
+            for (int c = 0; c < nch; ++c) do_stage(c, totA, totB);
+        } else {
+            // Eight partial sums, one per piece index mod 8: the blocks of
+            // partial j are exactly those warp j owns in a k-split launch,
+            // taken in the same order, and the partials are added in the
+            // same order as the k-split reduction.
+            float pa[GV_CONS], pb[GV_CONS];
 #pragma unroll
-        for (int c = 0; c < GV_CHUNK; ++c) {
-            if (kb0 + c >= kb_end) break;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint2* xb = &sm.xs[warp][c][0][0][0];
+            for (int j = 0; j < GV_CONS; ++j) pa[j] = pb[j] = 0.f;
+            for (int c0 = 0; c0 < nch; c0 += GV_CONS) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t wa = (s < 4) ? cA[c].x : cA[c].y;
-                const uint32_t wb = (s < 4) ? cB[c].x : cB[c].y;
-                uint32_t a[4];
-                switch (s & 3) {
-                    case 0: a[0] = opair<0>(wa); a[1] = opair<0>(wb); a[2] = opair<1>(wa); a[3] = opair<1>(wb); break;
-                    case 1: a[0] = opair<2>(wa); a[1] = opair<2>(wb); a[2] = opair<3>(wa); a[3] = opair<3>(wb); break;
-                    case 2: a[0] = opair<4>(wa); a[1] = opair<4>(wb); a[2] = opair<5>(wa); a[3] = opair<5>(wb); break;
-                    default: a[0] = opair<6>(wa); a[1] = opair<6>(wb); a[2] = opair<7>(wa); a[3] = opair<7>(wb); break;
-                }
-                uint2 b = make_uint2(0u, 0u);
-                if (g < 2 * MT) b = xb[(s * 2 * MT + g) * 4 + t];
-                mma_16816(acc, a, b.x, b.y, acc);
+                for (int j = 0; j < GV_CONS; ++j)
+                    if (c0 + j < nch) do_stage(c0 + j, pa[j], pb[j]);
             }
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (t == m) {
-                    const float corr = sm.corr[warp][c][m];
-                    totA[m] = fmaf(dA[c], (acc[0] + acc[1]) - corr, totA[m]);
-                    totB[m] = fmaf(dB[c], (acc[2] + acc[3]) - corr, totB[m]);
-                }
+            for (int j = 0; j < GV_CONS; ++j) {
+                totA += pa[j];
+                totB += pb[j];
+            }
         }
         __syncwarp();
-        if (kb0 + GV_CHUNK < kb_end) load_chunk(kb0 + GV_CHUNK);
-    }
-    // The next kernel may start launching now: this CTA's loads are done, and
-    // its prefetch cannot delay our (already finished) critical loads.
-    pdl_launch_dependents();
+        if (lane == 0) mbar_arrive(&sempty[slot]);
 
+        if (MODE == GV_ROWS) {
+            if (t < MT) {
+                const int ra = n0 + rbase + g;
+                if (ra < J.N) J.out[(int64_t)t * J.N + ra] = totA;
+                if (ra + 8 < J.N) J.out[(int64_t)t * J.N + ra + 8] = totB;
+            }
+        } else {
+            float* rd = red + (ui & 1) * (GV_CONS * 16 * MT);
+            if (t < MT) {
+                rd[(warp * 16 + g) * MT + t] = totA;
+                rd[(warp * 16 + g + 8) * MT + t] = totB;
+            }
+            consumers_sync();
+            if ((int)threadIdx.x < 16 * MT) {
+                const int m = threadIdx.x >> 4, r = threadIdx.x & 15;
+                float sum = 0.f;
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-        if (t == m) {
-            sm.red[warp][g][m] = totA[m];
-            sm.red[warp][g + 8][m] = totB[m];
+                for (int w = 0; w < GV_CONS; ++w) sum += rd[(w * 16 + r) * MT + m];
+                if (n0 + r < J.N) J.out[(int64_t)m * J.N + n0 + r] = sum;
+            }
         }
-    __syncthreads();
-    if (threadIdx.x < 16 * MT) {
-        const int m = threadIdx.x >> 4, r = threadIdx.x & 15;
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < GV_WARPS; ++w) s += sm.red[w][r][m];
-        if (n0 + r < N) out[(int64_t)m * N + n0 + r] = s;
     }
 }
 
-cudaError_t launch_gemv_table(const GemvTable& tab, int M, cudaStream_t st) {
-    const int ctas = tab.job[tab.njobs - 1].cta0 + (tab.job[tab.njobs - 1].N + 15) / 16;
-    const dim3 grid((unsigned)ctas), block(GV_WARPS * 32);
-    if (M == 1) return launch_pdl(tq2_gemv_kernel<1>, grid, block, 0, st, tab);
-    if (M == 2) return launch_pdl(tq2_gemv_kernel<2>, grid, block, 0, st, tab);
-    return cudaErrorInvalidValue;
+namespace {
+
+// Ring depth and scale slots for a mode: as many stages as fit beside a
+// second CTA (else alone); enough scale slots that the code ring, not the
+// scales, limits how far the producer runs ahead.  False if nothing fits.
+bool gv_plan(int K, int MT, int mode, int& stages, int& sslots) {
+    sslots = 2;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int fixed = (int)gv_layout(K, MT, mode, 0, sslots).total;
+        stages = (GV_SMEM_PAIR - fixed) / GV_STAGE;
+        if (stages < 4) stages = (GV_SMEM_MAX - fixed) / GV_STAGE;
+        if (stages > GV_MAX_STAGES) stages = GV_MAX_STAGES;
+        if (stages < 2) return false;
+        if (pass == 0) {
+            const int nch = (K / 128 + gv_stage_blocks(mode) - 1) / gv_stage_blocks(mode);
+            sslots = (stages + nch - 1) / nch + 1;
+            if (sslots > GV_MAX_SSLOTS) sslots = GV_MAX_SSLOTS;
+        }
+    }
+    return true;
 }
 
-cudaError_t launch_gemv(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M, int N,
-                        int K, cudaStream_t st) {
-    GemvTable tab;
-    tab.njobs = 1;
+template <int MT, int MODE, int NJ>
+cudaError_t gv_launch(const GemvTab<NJ>& tab, int units, int stages, int sslots, int sms, int dev,
+                      cudaStream_t st) {
+    static bool configured[64] = {false};
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tq2_gemv_kernel<MT, MODE, NJ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, GV_SMEM_MAX);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    // k-split: at most one CTA per SM while that leaves each only a few units
+    // (the next kernel on the stream then fits beside it); otherwise two per
+    // SM, since eight consumer warps alone do not hide the MMA and load latency.
+    const int slots = (MODE == GV_ROWS || units >= 8 * sms) ? 2 * sms : sms;
+    const int per = (units + slots - 1) / slots;
+    const int grid = (units + per - 1) / per;
+    const GvLayout L = gv_layout(tab.K, MT, MODE, stages, sslots);
+    return launch_pdl(tq2_gemv_kernel<MT, MODE, NJ>, dim3((unsigned)grid), dim3(GV_THREADS), (size_t)L.total, st,
+                      tab, units, stages, sslots);
+}
+
+template <int NJ>
+cudaError_t gv_dispatch(const tq2_weight* const* ws, const float* const* xs, float* const* outs, int G, int M,
+                        cudaStream_t st) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int K = (int)ws[0]->K;
+    int64_t units_r = 0;
+    for (int g = 0; g < G; ++g) units_r += (ws[g]->N + gv_unit_rows(GV_ROWS) - 1) / gv_unit_rows(GV_ROWS);
+    int stages = 0, sslots = 0;
+    int mode = GV_KSPLIT;
+    if (units_r >= sms && gv_plan(K, M, GV_ROWS, stages, sslots)) mode = GV_ROWS;
+    else if (!gv_plan(K, M, GV_KSPLIT, stages, sslots)) return cudaErrorInvalidValue;
+
+    GemvTab<NJ> tab;
+    tab.njobs = G;
     tab.K = K;
-    tab.job[0] = GemvJob{codes, scales, x, out, N, 0};
-    return launch_gemv_table(tab, M, st);
+    int64_t units = 0;
+    for (int g = 0; g < G; ++g) {
+        const tq2_weight* w = ws[g];
+        tab.job[g].map = mode == GV_ROWS ? w->gemv_map_r : w->gemv_map_k;
+        tab.job[g].scales = w->scales;
+        tab.job[g].x = xs[g];
+        tab.job[g].out = outs[g];
+        tab.job[g].N = (int)w->N;
+        tab.job[g].unit0 = (int)units;
+        units += (w->N + gv_unit_rows(mode) - 1) / gv_unit_rows(mode);
+    }
+    if (M == 1)
+        return mode == GV_ROWS ? gv_launch<1, GV_ROWS>(tab, (int)units, stages, sslots, sms, dev, st)
+                               : gv_launch<1, GV_KSPLIT>(tab, (int)units, stages, sslots, sms, dev, st);
+    return mode == GV_ROWS ? gv_launch<2, GV_ROWS>(tab, (int)units, stages, sslots, sms, dev, st)
+                           : gv_launch<2, GV_KSPLIT>(tab, (int)units, stages, sslots, sms, dev, st);
+}
+
+bool make_map(tq2_weight* w, CUtensorMap* map, uint32_t rows, uint32_t pieces) {
+    const uint64_t npieces = (uint64_t)(w->K / 4 + GV_PIECE - 1) / GV_PIECE;
+    const uint64_t dims[3] = {(uint64_t)GV_PIECE, (uint64_t)w->N, npieces};
+    const uint64_t strides[2] = {(uint64_t)(w->K / 4), (uint64_t)GV_PIECE};
+    const uint32_t box[3] = {(uint32_t)GV_PIECE, rows, pieces};
+    return make_tensor_map_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->codes, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+bool gemv_supports(int M, int64_t K) {
+    return M >= 1 && M <= GEMV_MAX_M && K >= 128 && (int64_t)M * K <= GEMV_MAX_MK;
+}
+
+bool make_gemv_maps(tq2_weight* w) {
+    return make_map(w, &w->gemv_map_k, 16u, (uint32_t)GV_CONS) &&
+           make_map(w, &w->gemv_map_r, (uint32_t)gv_unit_rows(GV_ROWS), 1u);
+}
+
+cudaError_t launch_gemv(const tq2_weight* const* ws, const float* const* xs, float* const* outs, int G, int M,
+                        cudaStream_t st) {
+    if (G < 1 || G > GEMV_MAX_JOBS || !gemv_supports(M, ws[0]->K)) return cudaErrorInvalidValue;
+    if (G == 1) return gv_dispatch<1>(ws, xs, outs, G, M, st);
+    return gv_dispatch<GEMV_MAX_JOBS>(ws, xs, outs, G, M, st);
+}
+
+unsigned int read_clear_dev_error_gemv(cudaStream_t st) {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_dev_error, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return 0;
+    cudaMemcpyToSymbolAsync(g_dev_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+    cudaStreamSynchronize(st);
+    return v;
 }
 
 }  // namespace tq2

@@ -9,11 +9,13 @@
 
 struct tq2_weight {
     int64_t N = 0, K = 0;
-    uint8_t* codes = nullptr;      // [N][K/4]
-    uint16_t* scales = nullptr;    // [N][K/128] f16 bits
+    uint8_t* codes = nullptr;      // [N][K/4], then 128 bytes of padding
+    uint16_t* scales = nullptr;    // [N][K/128] f16 bits, then 16 bytes of padding
     int device = 0;
-    CUtensorMap codes_map;         // 2D map over the code plane (bytes), built at upload
-    bool has_codes_map = false;
+    // 3D views of the code plane for the GEMV's TMA loads, built at upload:
+    // (128-byte piece, row, piece index), strides (1, K/4, 128) bytes; boxes
+    // of 16 rows x 8 pieces (k-split units) and 128 rows x 1 piece (row units).
+    CUtensorMap gemv_map_k, gemv_map_r;
 };
 
 namespace tq2 {
@@ -49,26 +51,17 @@ cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const fl
                           int N, int K, void* scratch, cudaStream_t st);
 unsigned int read_clear_dev_error_skinny(cudaStream_t st);
 
-// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M (no scratch); one launch may
-// run up to GEMV_MAX_JOBS independent GEMVs of the same K and M.
+// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M and M*K <= GEMV_MAX_MK (no
+// scratch; x lives in shared memory); one launch runs G <= GEMV_MAX_JOBS
+// independent GEMVs of the same K and M.
 constexpr int GEMV_MAX_M = 2;
+constexpr int64_t GEMV_MAX_MK = 32768;
 constexpr int GEMV_MAX_JOBS = 64;
-struct GemvJob {
-    const uint8_t* codes;
-    const uint16_t* scales;
-    const float* x;
-    float* out;
-    int N;
-    int cta0;     // first CTA of this job in the launch
-};
-struct GemvTable {
-    GemvJob job[GEMV_MAX_JOBS];
-    int njobs;
-    int K;
-};
-cudaError_t launch_gemv_table(const GemvTable& tab, int M, cudaStream_t st);
-cudaError_t launch_gemv(const uint8_t* codes, const uint16_t* scales, const float* x, float* out, int M, int N,
-                        int K, cudaStream_t st);
+bool gemv_supports(int M, int64_t K);
+bool make_gemv_maps(tq2_weight* w);
+cudaError_t launch_gemv(const tq2_weight* const* ws, const float* const* xs, float* const* outs, int G, int M,
+                        cudaStream_t st);
+unsigned int read_clear_dev_error_gemv(cudaStream_t st);
 
 // tq2_umma.cu
 size_t tensor_scratch_bytes(int64_t M, int64_t K);
@@ -88,5 +81,8 @@ int set_error(int st, const char* fmt, ...);
 bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                         CUtensorMapSwizzle swizzle);
+// 3D tiled map: dims[0] innermost (unit stride), strides of dims 1 and 2 in bytes.
+bool make_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle);
 
 }  // namespace tq2

@@ -104,7 +104,8 @@ TQ2_API tq2_status tq2_device_status(void* stream);
  *
  * Device layout behind the handle ("SoA"): a code plane uint8[N][K/4]
  * holding each row's qs bytes in K order, and a scale plane uint16[N][K/128]
- * of f16 bits.  Codes are not validated: code 3 decodes as +2 (3-1).
+ * of f16 bits, each followed by a little zeroed padding.  Codes are not
+ * validated: code 3 decodes as +2 (3-1).
  */
 TQ2_API tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, void* stream);
 
@@ -131,7 +132,7 @@ TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
  *
  * M <= 16 runs the skinny kernel: f32 activations split exactly into two
  * f16 terms, f32 accumulation; |error| <= 1e-3 at K <= 4096 for unit-scale
- * data.  M > 16 runs the tensor-core kernel: activations rounded to f16
+ * data.  For M <= 2 and M*K <= 32768 it is a single kernel with no scratch.  M > 16 runs the tensor-core kernel: activations rounded to f16
  * (nearest-even), weights exact in f16, f32 accumulation;
  * |error| <= 1e-2 * sum_k |x[m,k] W[n,k]|.
  */
@@ -154,7 +155,8 @@ TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64
  *   hs      HOST array of G handles; all must have the same K.
  *   xs      HOST array of G DEVICE pointers, float[M][K] each, 16-byte aligned.
  *   outs    HOST array of G DEVICE pointers, float[M][N_g] each (overwritten).
- *   G       1..64;  M in {1, 2};  K the handles' K.  Else TQ2_ESHAPE.
+ *   G       1..64;  M in {1, 2} with M*K <= 32768 (x is held in shared
+ *           memory);  K the handles' K.  Else TQ2_ESHAPE.
  *   stream  asynchronous; no scratch is allocated.
  */
 TQ2_API tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float* const* outs, int G,

@@ -33,7 +33,7 @@ def oracle_gemm(aos, N, K, x):
     return otq2.gemm(x64, W), otq2.gemm_abs(x64, W), otq2.gemm(x16, W), otq2.gemm_abs(x16, W)
 
 
-# Bounds ("Tolerances"):
+# Bounds:
 #  skinny: |err| <= 1e-3 (pages, K <= 4096) and |err| <= 2^-12 * sum|x W| + 1e-7
 #          (f32 accumulation over K <= 4096 terms, plus the 2^-22 split residual)
 #  tensor: |err| <= 1e-2 * sum|x W| against the exact oracle (required), and

@@ -1,8 +1,8 @@
 """GPU parity of the blr layer (bitmap expansion, forward, backward) through
 the C ABI against the f64 oracle.
 
-Bounds ("cortiq-engine 0.8.43, train_mm.rs", test blr_layer_matches_host, and
-DESIGN.md "Tolerances"): relative L2 error < 3e-3 per tensor (the page's
+Bounds ("cortiq-engine 0.8.43, train_mm.rs", test blr_layer_matches_host):
+relative L2 error < 3e-3 per tensor (the page's
 bound) and, per element, |gpu - oracle| <= 2^-9 * (the absolute-value chain
 of the same expression).  Each output passes through at most two f16
 roundings (2 * 2^-11) plus f32 accumulation over at most 4096 + 512 terms.

@@ -64,7 +64,7 @@ def test_tiny_skinny_page_activations(tiny, lib):
         check_skinny(got, ref, absref, f"page x M={M}")
 
 
-@pytest.mark.parametrize("N,K", [(8, 128), (40, 256), (3072, 3072), (17, 1152)])
+@pytest.mark.parametrize("N,K", [(8, 128), (40, 256), (3072, 3072), (17, 1152), (33, 2176)])
 def test_skinny_page_sweep(lib, N, K):
     aos = page_sweep_weight(N, K)
     w = lib.tq2_upload(aos, N, K)
@@ -124,6 +124,75 @@ def test_gemv_grouped_matches_single_calls(lib):
     with pytest.raises(lib.TQ2Error):                       # M = 3 is not a grouped shape
         x3 = [torch.zeros((3, K), device="cuda") for _ in ws]
         lib.tq2_gemm_grouped(ws, x3, [torch.zeros((3, w.N), device="cuda") for w in ws])
+
+
+def test_gemv_many_units_per_cta_sampled(lib):
+    """N = 30000 rows at K = 4096: every CTA of the fused GEMV walks several
+    units and the stage ring and scale slots wrap many times.  Sampled rows
+    (all of the first and last few) against the oracle, element by element."""
+    import torch
+    N, K = 30000, 4096
+    aos = synth.random_tq2(N, K, 92)
+    w = lib.tq2_upload(aos, N, K)
+    codes, d_bits = otq2.parse_aos(aos, N, K)
+    rng = np.random.Generator(np.random.Philox(key=93))
+    rows = sorted(set(rng.integers(0, N, 600).tolist()) | set(range(20)) | set(range(N - 20, N)))
+    for M in (1, 2):
+        x = synth.random_x(M, K, 94 + M)
+        xd = to_dev(x)
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        lib.tq2_gemm(w, xd, out)
+        lib.device_status()
+        assert not torch.isnan(out).any().item()
+        got = out.cpu().numpy().astype(np.float64)
+        for m in range(M):
+            for n in rows:
+                ref, absref = otq2.gemm_elem(x[m], codes[n], d_bits[n])
+                err = abs(got[m, n] - ref)
+                assert err <= 1e-3 and err <= 2.0 ** -12 * absref + 1e-7, (m, n, got[m, n], ref)
+
+
+def test_gemv_grouped_64_jobs_bit_identical(lib):
+    """64 jobs of N=4096, K=4096 (the decode-shape workload) in one launch:
+    each CTA walks many row groups; every output equals the single call."""
+    import torch
+    N, K = 4096, 4096
+    ws = [lib.tq2_upload(synth.random_tq2(N, K, 100 + i), N, K) for i in range(4)]
+    hs = [ws[i % 4] for i in range(64)]
+    xs = [to_dev(synth.random_x(1, K, 200 + (i % 8))) for i in range(64)]
+    outs = [torch.full((1, N), float("nan"), device="cuda") for _ in range(64)]
+    lib.tq2_gemm_grouped(hs, xs, outs)
+    lib.device_status()
+    for i in range(64):
+        single = torch.empty_like(outs[i])
+        lib.tq2_gemm(hs[i], xs[i], single)
+        lib.device_status()
+        assert torch.equal(outs[i], single), i
+
+
+def test_gemv_mk_limit(lib):
+    """M * K above the shared-memory limit of the fused GEMV: a single call
+    falls back to the staged skinny kernel, a grouped call is refused."""
+    import torch
+    N, K = 40, 16512                     # M = 2: M * K = 33024 > 32768
+    aos = synth.random_tq2(N, K, 95)
+    w = lib.tq2_upload(aos, N, K)
+    for M in (1, 2):
+        x = synth.random_x(M, K, 96) * 0.5
+        got = run_gemm(lib, w, x)
+        ref, absref, _, _ = oracle_gemm(aos, N, K, x)
+        assert np.max(np.abs(got - ref)) <= 2e-3
+        assert np.all(np.abs(got - ref) <= (2.0 ** -10) * absref + 1e-7)
+    x2 = torch.zeros((2, K), device="cuda")
+    with pytest.raises(lib.TQ2Error):
+        lib.tq2_gemm_grouped([w], [x2], [torch.zeros((2, N), device="cuda")])
+    x1 = to_dev(synth.random_x(1, K, 97))
+    o1 = torch.empty((1, N), device="cuda")
+    lib.tq2_gemm_grouped([w], [x1], [o1])                       # M = 1 fits
+    lib.device_status()
+    single = torch.empty_like(o1)
+    lib.tq2_gemm(w, x1, single)
+    assert torch.equal(o1, single)
 
 
 def test_gemv_full_size(lib):
