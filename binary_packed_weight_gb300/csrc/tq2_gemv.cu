@@ -102,16 +102,32 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_
 //   word: <<4 <<4  .   .   .  >>6 >>6 >>6
 //   P:    4   6   4   6   8   4   6   8
 //   m_q:  64  16  64  16  4   64  16  4
+// The integer ALU pipe runs at half rate and is the decode's bottleneck, so:
+//   * the two shifts are integer multiplies (w * 16, and the high half of
+//     w * 2^26) by factors the compiler cannot fold, which run on the FMA pipe;
+//   * the three masks sit in registers, so (w & mask) | magic is a single
+//     three-input logic op with the magic as its one immediate.
+struct GvShift {
+    uint32_t m16, m2p26;         // 16 and 2^26
+    uint32_t k4, k6, k8;         // 0x00030003 << 4, << 6, << 8
+};
+template <int P>
+__device__ __forceinline__ uint32_t gv_op(uint32_t ws, uint32_t mask) {
+    constexpr uint32_t mh = (uint32_t)(25 - P) << 10;     // f16 bits of 2^(10-P)
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(ws), "r"(mask), "n"(mh | (mh << 16)));   // (a & b) | c
+    return r;
+}
 template <int Q>
-__device__ __forceinline__ uint32_t gv_pair(uint32_t w) {
-    if constexpr (Q == 0) return offset_pair<4>(w << 4);
-    else if constexpr (Q == 1) return offset_pair<6>(w << 4);
-    else if constexpr (Q == 2) return offset_pair<4>(w);
-    else if constexpr (Q == 3) return offset_pair<6>(w);
-    else if constexpr (Q == 4) return offset_pair<8>(w);
-    else if constexpr (Q == 5) return offset_pair<4>(w >> 6);
-    else if constexpr (Q == 6) return offset_pair<6>(w >> 6);
-    else return offset_pair<8>(w >> 6);
+__device__ __forceinline__ uint32_t gv_pair(uint32_t w, uint32_t wl, uint32_t wr, const GvShift& sh) {
+    if constexpr (Q == 0) return gv_op<4>(wl, sh.k4);
+    else if constexpr (Q == 1) return gv_op<6>(wl, sh.k6);
+    else if constexpr (Q == 2) return gv_op<4>(w, sh.k4);
+    else if constexpr (Q == 3) return gv_op<6>(w, sh.k6);
+    else if constexpr (Q == 4) return gv_op<8>(w, sh.k8);
+    else if constexpr (Q == 5) return gv_op<4>(wr, sh.k4);
+    else if constexpr (Q == 6) return gv_op<6>(wr, sh.k6);
+    else return gv_op<8>(wr, sh.k8);
 }
 // m_q + 1 for the element at position e (0..15) of a word.
 __host__ __device__ constexpr float gv_plus_one(int e) {
@@ -121,11 +137,18 @@ __host__ __device__ constexpr float gv_plus_one(int e) {
 // The A fragment of k16 step j (0..3) of a word: rows g and g+8 from words
 // wa and wb; positions 2t,2t+1 hold pair 2j, positions 2t+8,2t+9 pair 2j+1.
 template <int J>
-__device__ __forceinline__ void gv_afrag(uint32_t wa, uint32_t wb, uint32_t (&a)[4]) {
-    a[0] = gv_pair<2 * J>(wa);
-    a[1] = gv_pair<2 * J>(wb);
-    a[2] = gv_pair<2 * J + 1>(wa);
-    a[3] = gv_pair<2 * J + 1>(wb);
+__device__ __forceinline__ void gv_afrag(const uint32_t (&wa)[3], const uint32_t (&wb)[3], uint32_t (&a)[4],
+                                         const GvShift& sh) {
+    a[0] = gv_pair<2 * J>(wa[0], wa[1], wa[2], sh);
+    a[1] = gv_pair<2 * J>(wb[0], wb[1], wb[2], sh);
+    a[2] = gv_pair<2 * J + 1>(wa[0], wa[1], wa[2], sh);
+    a[3] = gv_pair<2 * J + 1>(wb[0], wb[1], wb[2], sh);
+}
+// A word with its two shifted copies: w, w << 4, w >> 6.
+__device__ __forceinline__ void gv_word(uint32_t w, const GvShift& sh, uint32_t (&o)[3]) {
+    o[0] = w;
+    o[1] = w * sh.m16;
+    o[2] = __umulhi(w, sh.m2p26);
 }
 
 struct GvLayout {
@@ -143,7 +166,8 @@ __host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stage
     L.off_sc = L.off_corr + (((uint32_t)L.nb + 3u) & ~3u) * MT * 4;             // whole pieces (float4 reads)
     L.sc_bytes = ((uint32_t)gv_unit_rows(mode) * L.nb * 2 + 16u + 15u) & ~15u;
     L.off_xs = L.off_sc + (uint32_t)sslots * L.sc_bytes;
-    L.off_ring = L.off_xs + (uint32_t)L.nb * 8 * (2 * MT) * 4 * 8;              // [nb][2MT][4][8] uint2
+    // [nb rounded up to whole pieces][4 step pairs][2MT][4] uint4
+    L.off_ring = L.off_xs + (((uint32_t)L.nb + 3u) & ~3u) * 4 * (2 * MT) * 4 * 16;
     L.total = L.off_ring + 1024u + (uint32_t)stages * GV_STAGE;                  // + room to align to 1 KB
     return L;
 }
@@ -153,37 +177,41 @@ __host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stage
 // 16-byte chunk (2i + t/2) of a 128-byte row is stored at chunk
 // (2i + t/2) ^ (row & 7), and row g+8 sits 1 KB after row g.  scA points at
 // row g's scales (row g+8's are 8*nb further).  x fragments are stored
-// [block][column][t][k16 step] (uint2), so one 16-byte load serves two
-// steps; each block's eight MMAs form one accumulator chain, the four
-// blocks' chains interleave.
+// [block][k16 step pair][column][t] (uint4 = two steps' b0,b1), so the
+// lanes of one load read 16 * 8 * MT contiguous bytes; xl is this lane's
+// fragment base, xstep / sstep its strides per block / step pair.  Lanes
+// g >= 2MT supply B columns whose D columns are never read, so they load
+// another lane's fragment (a broadcast).  Each block's eight MMAs form one
+// accumulator chain; the four blocks' chains interleave.
 template <int MT>
-__device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const uint2* xs, const float* corr,
-                                         int blk0, int nv, int nb, const uint16_t* scA, int tm, float& totA,
-                                         float& totB) {
-    uint2 ca[GV_BPW], cb[GV_BPW];
-    const uint4* xb[GV_BPW];
+__device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const uint4* xl, int xstep, int sstep,
+                                         const float* corr, int blk0, int nv, int nb, const uint16_t* scA, int tm,
+                                         const GvShift& sh, float& totA, float& totB) {
+    uint32_t wa[GV_BPW][2][3], wb[GV_BPW][2][3];
+    const uint4* xb = xl + blk0 * xstep;
 #pragma unroll
     for (int i = 0; i < GV_BPW; ++i) {
         const uint8_t* p = pc + ((((2 * i + (t >> 1)) ^ g) & 7) << 4);
-        ca[i] = *reinterpret_cast<const uint2*>(p);
-        cb[i] = *reinterpret_cast<const uint2*>(p + 8 * GV_PIECE);
-        xb[i] = reinterpret_cast<const uint4*>(xs + ((min(blk0 + i, nb - 1) * (2 * MT) + g) * 4 + t) * 8);
+        const uint2 ca = *reinterpret_cast<const uint2*>(p);
+        const uint2 cb = *reinterpret_cast<const uint2*>(p + 8 * GV_PIECE);
+        gv_word(ca.x, sh, wa[i][0]);
+        gv_word(ca.y, sh, wa[i][1]);
+        gv_word(cb.x, sh, wb[i][0]);
+        gv_word(cb.y, sh, wb[i][1]);
     }
     float acc[GV_BPW][4];
 #pragma unroll
     for (int i = 0; i < GV_BPW; ++i)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
-    const bool bl = g < 2 * MT;
     // steps 0-3 decode word x (k 32t..32t+15 of the block), 4-7 word y
 #define GV_STEP2(S)                                                                         \
     _Pragma("unroll") for (int i = 0; i < GV_BPW; ++i) {                                    \
-        const uint4 b = bl ? xb[i][(S) / 2] : make_uint4(0u, 0u, 0u, 0u);                   \
-        const uint32_t w0 = (S) < 4 ? ca[i].x : ca[i].y, w1 = (S) < 4 ? cb[i].x : cb[i].y;   \
+        const uint4 b = xb[i * xstep + ((S) / 2) * sstep];                                  \
         uint32_t a[4];                                                                      \
-        gv_afrag<(S) % 4>(w0, w1, a);                                                       \
+        gv_afrag<(S) % 4>(wa[i][(S) / 4], wb[i][(S) / 4], a, sh);                           \
         mma_16816_pure(acc[i], a, b.x, b.y);                                                \
-        gv_afrag<((S) + 1) % 4>(w0, w1, a);                                                 \
+        gv_afrag<((S) + 1) % 4>(wa[i][(S) / 4], wb[i][(S) / 4], a, sh);                     \
         mma_16816_pure(acc[i], a, b.z, b.w);                                                \
     }
     GV_STEP2(0)
@@ -247,7 +275,7 @@ __global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab
     float* red = reinterpret_cast<float*>(smem + L.off_red);       // [2][GV_CONS][16][MT] (k-split)
     float* corr = reinterpret_cast<float*>(smem + L.off_corr);     // [nb][MT]
     uint8_t* scb = smem + L.off_sc;                                // [sslots] x ([UR][nb] f16)
-    uint2* xs = reinterpret_cast<uint2*>(smem + L.off_xs);         // [nb][2MT][4][8]
+    uint2* xs = reinterpret_cast<uint2*>(smem + L.off_xs);         // [nb][4][2MT][4][2]
     // [stages][8 warps][16 rows][128 B], 1 KB aligned for the 128-byte swizzle
     uint8_t* ring = smem + L.off_ring + ((1024u - ((smem_u32(smem) + L.off_ring) & 1023u)) & 1023u);
 
@@ -286,27 +314,28 @@ __global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab
     if (warp == GV_CONS) {
         // ------------------------------------------------ producer warp ----
         if (lane != 0) return;
-        int it = 0, job = 0;
+        int it = 0, job = 0, s = 0, slot = 0;
+        uint32_t ph = 0, sph = 0;                // phase parity of the current ring / slot round
         bool ok = true;
         for (int u = u_begin, ui = 0; u < u_end && ok; ++u, ++ui) {
             int n0;
             locate(u, job, n0);
             const GvJobS& J = sj[job];
             const int rows = min(UR, J.N - n0);
-            const int slot = ui % sslots;
-            if (ui >= sslots) ok = mbar_wait(&sempty[slot], ((ui / sslots) - 1) & 1);
+            if (ui >= sslots) ok = mbar_wait(&sempty[slot], sph ^ 1u);
             if (!ok) break;
             // rounded up to 16 bytes: the scale plane carries 16 bytes of padding
             const uint32_t sbytes = ((uint32_t)rows * nb * 2 + 15u) & ~15u;
             mbar_arrive_expect_tx(&sfull[slot], sbytes);
             bulk_load(scb + slot * L.sc_bytes, J.scales + (int64_t)n0 * nb, sbytes, &sfull[slot]);
+            if (++slot == sslots) { slot = 0; sph ^= 1u; }
             for (int c = 0; c < nch; ++c, ++it) {
-                const int s = it % stages;
-                if (it >= stages) ok = mbar_wait(&empty[s], ((it / stages) - 1) & 1);
+                if (it >= stages) ok = mbar_wait(&empty[s], ph ^ 1u);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)GV_STAGE);
                 tma_load_3d(ring + s * GV_STAGE, &tab.job[job].map, &full[s], 0, n0,
                             MODE == GV_ROWS ? c : c * GV_CONS);
+                if (++s == stages) { s = 0; ph ^= 1u; }
             }
         }
         return;
@@ -359,9 +388,10 @@ __global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab
                         uint32_t h01, l01, h23, l23;
                         split2(e[2 * j], e[2 * j + 8], h01, l01);
                         split2(e[2 * j + 1], e[2 * j + 9], h23, l23);
-                        uint2* d = xs + ((blk * (2 * MT) + 2 * m) * 4 + st_t) * 8 + 4 * st_y + j;
+                        // step 4y + j -> pair 2y + j/2, half j % 2
+                        uint2* d = xs + (((blk * 4 + 2 * st_y + (j >> 1)) * (2 * MT) + 2 * m) * 4 + st_t) * 2 + (j & 1);
                         d[0] = make_uint2(h01, h23);              // column 2m: hi
-                        d[32] = make_uint2(l01, l23);             // column 2m+1: lo
+                        d[8] = make_uint2(l01, l23);              // column 2m+1: lo
                     }
                 }
                 cs += __shfl_xor_sync(0xffffffffu, cs, 1);
@@ -375,27 +405,33 @@ __global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab
         staged = x;
     };
 
-    int it = 0, job = 0;
+    // this lane's x fragments: column g < 2MT, else the zero area
+    // this lane's x fragments (uint4 units); lanes g >= 2MT alias column g % 2MT
+    const int xstep = 4 * (2 * MT) * 4, sstep = (2 * MT) * 4;
+    const uint4* xl = reinterpret_cast<const uint4*>(xs) + (g % (2 * MT)) * 4 + t;
+    const uint32_t z = (uint32_t)(K >> 30);      // 0 (K < 2^30), opaque to the compiler
+    const GvShift sh{16u | z, (1u << 26) | z, 0x00300030u | z, 0x00C000C0u | z, 0x03000300u | z};
+
+    int s = 0, slot = 0, job = 0;
+    uint32_t ph = 0, sph = 0;
     bool dead = false;                            // a bounded wait ran out: skip the rest
     const int rbase = MODE == GV_ROWS ? 16 * warp : 0;
-    for (int u = u_begin, ui = 0; u < u_end; ++u, ++ui) {
+    for (int u = u_begin; u < u_end; ++u) {
         int n0;
         locate(u, job, n0);
         const GvJobS& J = sj[job];
         if (J.x != staged) stage_x(J.x);
-        const int slot = ui % sslots;
-        if (!dead && !mbar_wait(&sfull[slot], (ui / sslots) & 1)) dead = true;
+        if (!dead && !mbar_wait(&sfull[slot], sph)) dead = true;
         const uint16_t* scA = reinterpret_cast<const uint16_t*>(scb + slot * L.sc_bytes) + (rbase + g) * nb;
         auto do_stage = [&](int c, float& ta, float& tb) {
-            const int s = it % stages;
-            if (!dead && !mbar_wait(&full[s], (it / stages) & 1)) dead = true;
+            if (!dead && !mbar_wait(&full[s], ph)) dead = true;
             const uint8_t* pc = ring + s * GV_STAGE + warp * GV_WARP_BYTES + g * GV_PIECE + 8 * (t & 1);
             const int blk0 = MODE == GV_ROWS ? GV_BPW * c : c * (GV_BPW * GV_CONS) + GV_BPW * warp;
             const int nv = min(GV_BPW, nb - blk0);              // valid blocks (warp-uniform)
-            if (!dead && nv > 0) gv_piece<MT>(pc, g, t, xs, corr, blk0, nv, nb, scA, tm, ta, tb);
+            if (!dead && nv > 0) gv_piece<MT>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            ++it;
+            if (++s == stages) { s = 0; ph ^= 1u; }
         };
         float totA = 0.f, totB = 0.f;            // rows rbase+g and rbase+g+8, token tm
         if (MODE == GV_KSPLIT) {
@@ -421,6 +457,8 @@ __global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[slot]);
+        const int ui = u - u_begin;
+        if (++slot == sslots) { slot = 0; sph ^= 1u; }
 
         if (MODE == GV_ROWS) {
             if (t < MT) {
