@@ -259,9 +259,12 @@ __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const 
 
 }  // namespace
 
-// 112 registers: two CTAs of 288 threads fill the register file exactly.
+// Registers: row-split launches run two CTAs per SM, and 18 warps spread over
+// four 16K-register sub-partitions fit only at <= 96 registers a thread;
+// k-split launches keep one CTA per SM (plus the next kernel's, when it fits)
+// and take 112.
 template <int MT, int MODE, int NJ>
-__global__ void __maxnreg__(112) tq2_gemv_kernel(const __grid_constant__ GemvTab<NJ> tab, int units, int stages,
+__global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __grid_constant__ GemvTab<NJ> tab, int units, int stages,
                                                  int sslots) {
     constexpr int UR = gv_unit_rows(MODE);
     extern __shared__ __align__(128) uint8_t smem[];
@@ -513,6 +516,11 @@ cudaError_t gv_launch(const GemvTab<NJ>& tab, int units, int stages, int sslots,
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(tq2_gemv_kernel<MT, MODE, NJ>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, GV_SMEM_MAX);
+        // row-split: ask for the largest shared-memory carveout so that two
+        // CTAs fit on an SM (the default picks one just large enough for one)
+        if (e == cudaSuccess && MODE == GV_ROWS)
+            e = cudaFuncSetAttribute(tq2_gemv_kernel<MT, MODE, NJ>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
