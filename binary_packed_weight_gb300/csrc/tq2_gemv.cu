@@ -183,7 +183,7 @@ __host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stage
 // g >= 2MT supply B columns whose D columns are never read, so they load
 // another lane's fragment (a broadcast).  Each block's eight MMAs form one
 // accumulator chain; the four blocks' chains interleave.
-template <int MT>
+template <int MT, bool FULL>
 __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const uint4* xl, int xstep, int sstep,
                                          const float* corr, int blk0, int nv, int nb, const uint16_t* scA, int tm,
                                          const GvShift& sh, float& totA, float& totB) {
@@ -250,7 +250,7 @@ __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const 
     }
 #pragma unroll
     for (int i = 0; i < GV_BPW; ++i) {
-        if (i < nv) {
+        if (FULL || i < nv) {
             totA = fmaf(dA[i], (acc[i][0] + acc[i][1]) - cr[i], totA);
             totB = fmaf(dB[i], (acc[i][2] + acc[i][3]) - cr[i], totB);
         }
@@ -427,11 +427,12 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
         if (!dead && !mbar_wait(&sfull[slot], sph)) dead = true;
         const uint16_t* scA = reinterpret_cast<const uint16_t*>(scb + slot * L.sc_bytes) + (rbase + g) * nb;
         auto do_stage = [&](int c, float& ta, float& tb) {
-            if (!dead && !mbar_wait(&full[s], ph)) dead = true;
+            if (!dead && !mbar_wait(&full[s], ph)) dead = true;   // after a timeout: no more waits
             const uint8_t* pc = ring + s * GV_STAGE + warp * GV_WARP_BYTES + g * GV_PIECE + 8 * (t & 1);
             const int blk0 = MODE == GV_ROWS ? GV_BPW * c : c * (GV_BPW * GV_CONS) + GV_BPW * warp;
             const int nv = min(GV_BPW, nb - blk0);              // valid blocks (warp-uniform)
-            if (!dead && nv > 0) gv_piece<MT>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
+            if (nv == GV_BPW) gv_piece<MT, true>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
+            else if (nv > 0) gv_piece<MT, false>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (++s == stages) { s = 0; ph ^= 1u; }
