@@ -3,10 +3,14 @@
 
 Headline workload: the TQ2 GEMV (decode shape) M=1, N=K=4096, codes iid
 uniform over {0,1,2}, per-block f16 scales iid U(0.01, 0.1), x iid N(0,1).
-One *step* is one CUDA-graph replay of 64 GEMVs, each against its own copy
-of the weight (64 x 4.46 MB = 285 MB > the 129 MB L2, so every GEMV streams
-its weight from HBM).  ``value`` is packed-weight GB/s over the whole job:
-(N*K/4 + N*K/128*2) bytes per GEMV x GEMVs / device time.
+One *step* is 64 such GEMVs, each against its own copy of the weight
+(64 x 4.46 MB = 285 MB > the 129 MB L2, so every GEMV streams its weight
+from HBM), issued as one tq2_gemm_grouped call (the library's call for
+independent GEMVs that share K and M).  ``value`` is packed-weight GB/s over
+the whole job: (N*K/4 + N*K/128*2) bytes per GEMV x GEMVs / device time.
+The same 64 GEMVs issued as 64 stream-ordered tq2_gemm calls (each waits
+for the one before it) are reported under ``extra`` as the latency-bound
+form.
 
 The same JSON line carries, under ``extra``, the other workloads of the hot
 path measured the same way (skinny M=8/32/128 x N=11008, large M=4096 x
@@ -38,7 +42,7 @@ GEMV_COPIES = 64
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
@@ -139,59 +143,79 @@ def gemv_bytes(N, K):
 
 
 # ------------------------------------------------------------- workloads ----
+def capture(torch, fn, stream, warmup):
+    with torch.cuda.stream(stream):
+        fn()                                   # first call outside capture (allocator pools)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
 def run_gemv(torch, bpw, args, stream, dev):
     cfg = synth.GEMV
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     aos = synth.random_tq2(N, K, cfg["wkey"])
     ws = [bpw.tq2_upload(aos, N, K) for _ in range(GEMV_COPIES)]
     x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
-    out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in ws]
+    xs = [x] * len(ws)
+
+    def grouped():
+        bpw.tq2_gemm_grouped(ws, xs, outs, stream=stream.cuda_stream)
+
+    g = capture(torch, grouped, stream, args.warmup)
+    clocks = Clocks(dev.index if dev.index is not None else 0)
+    return dict(ws=ws, x=x, xs=xs, outs=outs, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
+
+
+def extra_chained(torch, bpw, ctx, stream, pk):
+    """The same 64 GEMVs as 64 stream-ordered tq2_gemm calls (latency-bound:
+    each waits for the previous kernel; weights prefetch under PDL)."""
+    ws, x, N, K, M = ctx["ws"], ctx["x"], ctx["N"], ctx["K"], ctx["M"]
+    out = ctx["outs"][0]
 
     def step():
         for w in ws:
             bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
-
-    clocks = Clocks(dev.index if dev.index is not None else 0)
-    # capture + warm up, then the clocked, timed region
-    secs, g = None, None
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        step()
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            g.replay()
-    torch.cuda.synchronize()
-    return dict(ws=ws, x=x, out=out, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
+    secs, _ = time_graph(torch, step, 200, 5, stream)
+    t = secs / 200 / len(ws)
+    alg = gemv_bytes(N, K) + M * K * 4 + M * N * 4
+    return dict(us_per_gemv=t * 1e6, gemvs_per_step=len(ws), weight_gbs=gemv_bytes(N, K) / t / 1e9,
+                alg_gbs=alg / t / 1e9, hbm_frac=alg / t / 1e9 / pk["hbm"],
+                kernel="tq2_gemv_kernel<1, k-split, 1 job> (one launch per GEMV)")
 
 
 def e2e_gemv(torch, bpw, ctx, stream, reps):
-    """Public API with host buffers: pinned x -> device, tq2_gemm, out -> pinned host."""
+    """Public API with host buffers, every step: pinned x -> device, one
+    tq2_gemm_grouped call over the 64 weights, the 64 outputs -> pinned host."""
     M, N, K = ctx["M"], ctx["N"], ctx["K"]
+    ws, xs, outs = ctx["ws"], ctx["xs"], ctx["outs"]
     xh = torch.from_numpy(synth.random_x(M, K, synth.GEMV["xkey"])).pin_memory()
-    oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    xd, od = ctx["x"], ctx["out"]
-    for _ in range(3):
-        for w in ctx["ws"]:
-            with torch.cuda.stream(stream):
-                xd.copy_(xh, non_blocking=True)
-                bpw.tq2_gemm(w, xd, od, stream=stream.cuda_stream)
-                oh.copy_(od, non_blocking=True)
-    stream.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        for w in ctx["ws"]:
-            with torch.cuda.stream(stream):
-                xd.copy_(xh, non_blocking=True)
-                bpw.tq2_gemm(w, xd, od, stream=stream.cuda_stream)
+    ohs = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in ws]
+    xd = xs[0]
+
+    def step():
+        with torch.cuda.stream(stream):
+            xd.copy_(xh, non_blocking=True)
+            bpw.tq2_gemm_grouped(ws, xs, outs, stream=stream.cuda_stream)
+            for oh, od in zip(ohs, outs):
                 oh.copy_(od, non_blocking=True)
         stream.synchronize()
+    for _ in range(3):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        step()
     dt = time.perf_counter() - t0
-    n = reps * len(ctx["ws"])
+    n = reps * len(ws)
     return dict(value=gemv_bytes(N, K) * n / dt / 1e9, unit="GB/s",
-                h2d_bytes_per_step=M * K * 4 * len(ctx["ws"]), d2h_bytes_per_step=M * N * 4 * len(ctx["ws"]))
+                h2d_bytes_per_step=M * K * 4, d2h_bytes_per_step=M * N * 4 * len(ws))
 
 
 def extra_skinny(torch, bpw, stream, dev, pk, Ms):
@@ -221,23 +245,6 @@ def extra_skinny(torch, bpw, stream, dev, pk, Ms):
     for w in ws:
         w.free()
     return res
-
-
-def extra_grouped(torch, bpw, ctx, stream, pk):
-    """The same 64 GEMVs as one grouped launch (independent weights, shared x)."""
-    ws, x, N, K, M = ctx["ws"], ctx["x"], ctx["N"], ctx["K"], ctx["M"]
-    outs = [torch.empty((M, N), dtype=torch.float32, device=x.device) for _ in ws]
-    xs = [x] * len(ws)
-
-    def step():
-        bpw.tq2_gemm_grouped(ws, xs, outs, stream=stream.cuda_stream)
-    secs, _ = time_graph(torch, step, 200, 5, stream)
-    t = secs / 200
-    wb = gemv_bytes(N, K) * len(ws)
-    alg = wb + len(ws) * (M * K * 4 + M * N * 4)
-    return dict(us_per_launch=t * 1e6, gemvs_per_launch=len(ws), weight_gbs=wb / t / 1e9,
-                alg_gbs=alg / t / 1e9, hbm_frac=alg / t / 1e9 / pk["hbm"],
-                kernel="tq2_gemv_kernel<1> (table of 64 jobs)")
 
 
 def extra_blr(torch, bpw, stream, dev, pk):
@@ -380,18 +387,18 @@ def main():
     gemvs = args.steps * GEMV_COPIES
     wbytes = gemv_bytes(N, K)
     value = wbytes * gemvs * world / secs / 1e9
-    t_launch = secs / gemvs
-    alg = wbytes + M * K * 4 + M * N * 4
+    t_launch = secs / args.steps                      # one grouped launch per step
+    alg = GEMV_COPIES * (wbytes + M * K * 4 + M * N * 4)
     achieved = alg / t_launch / 1e9
-    e2e = e2e_gemv(torch, bpw, ctx, stream, reps=max(2, min(20, args.steps // 50)))
+    e2e = e2e_gemv(torch, bpw, ctx, stream, reps=max(20, min(200, args.steps // 10)))
 
     extra = {}
     if not args.no_extra and rank == 0:
         only = set(filter(None, args.only.split(",")))
         if not only or "skinny" in only:
             extra["tq2_skinny_N11008"] = extra_skinny(torch, bpw, stream, dev, pk, (8, 32, 128))
-        if not only or "grouped" in only:
-            extra["tq2_gemv_grouped_64"] = extra_grouped(torch, bpw, ctx, stream, pk)
+        if not only or "chained" in only:
+            extra["tq2_gemv_chained_64"] = extra_chained(torch, bpw, ctx, stream, pk)
         if not only or "large" in only:
             extra["tq2_large_M4096_N14336"] = extra_large(torch, bpw, stream, dev, pk)
         if not only or "blr" in only:
@@ -406,6 +413,7 @@ def main():
         ms_per_step=secs / args.steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="f32", data="synthetic",
         config={"workload": cfg_name, "gemvs_per_step": GEMV_COPIES,
+                "launch": "one tq2_gemm_grouped call per step (64 jobs, shared x)",
                 "l2": f"inputs larger than L2: {GEMV_COPIES} distinct weight copies "
                       f"({GEMV_COPIES * wbytes / 1e6:.0f} MB) rotated every step",
                 "weights": "packed BlockTQ2_0_g128, 2 bits + f16 scale per 128",
@@ -414,10 +422,10 @@ def main():
                 "parallelism": "replicas" if world > 1 else "single GPU"},
         tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
         roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                  "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv"),
-                  "kernel": "tq2_gemv_kernel<1> (one launch per GEMV, average over the timed graph replays)",
+                  "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv_grouped"),
+                  "kernel": "tq2_gemv_kernel<1, row-split, 64 jobs> (one launch per step)",
                   "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"] + " hbm_gbs (copy)"},
-        cpu_baseline=cb, e2e=e2e, gpu_launches=gemvs, clocks=clk, extra=extra,
+        cpu_baseline=cb, e2e=e2e, gpu_launches=args.steps, clocks=clk, extra=extra,
     )
     print(json.dumps(line), flush=True)
     if dist:
