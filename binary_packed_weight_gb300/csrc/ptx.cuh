@@ -90,6 +90,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// As mbar_wait, but polling without a suspend hint (the global timer is read
+// every 256 polls): for short producer/consumer hand-offs where a sleeping
+// waiter would wake up late.  Same 1 s bound and error record.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            record_timeout();
+            return false;
+        }
+    }
+}
+
+// Wait that also gives up when another role has set `abort_flag`; the flag
+// is read only while the phase is still pending, so the fast path is one
+// try_wait.  spin: poll without a suspend hint (for the MMA-issuing thread,
+// whose lateness idles the tensor pipe).  Same 1 s bound and error record.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   bool spin = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (spin ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+        if (*abort_flag) return false;
+        if ((spin ? (i & 255u) == 0 : true) && global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            record_timeout();
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA ----
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -231,6 +264,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
           "=r"(v[31])
         : "r"(taddr)
         : "memory");
+}
+
+// 32 lanes x 2 / 4 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x2(uint32_t taddr, uint32_t (&v)[2]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(taddr) : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA

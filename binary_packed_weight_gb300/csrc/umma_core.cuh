@@ -230,15 +230,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     if (warp == 0) {
         if (lane == 0) {                                   // ---- TMA producer
             pdl_wait();
-            int it = 0;
+            int it = 0, s = 0;
+            uint32_t ph = 0;                               // ring slot and phase parity of item `it`
             bool ok = true;
-            for (int t = unit0; t < tm.total && ok; t += units) {
+            for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
                 for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (uint32_t)(it / S) & 1u;
-                    if ((it >= S && !mbar_wait(&bars->empty[s], ph ^ 1u)) || *abort_flag) {
+                    if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -250,6 +249,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                                        m * BN + rank * part, cmask);
                     else
                         tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full_b[s], kc * UM_BK, m * BN);
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
             // let the copies already issued land before the CTA can exit
@@ -259,23 +259,23 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     } else if (warp == 1) {
         if (lane == 0) {                                   // ---- MMA issuer
             const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
-            int it = 0, lt = 0;
+            int lt = 0, s = 0;
+            uint32_t ph = 0;
             bool ok = true;
-            for (int t = unit0; t < tm.total && ok; t += units, ++lt) {
+            for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units, ++lt) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
-                const int buf = lt % NACC, use = lt / NACC;
-                if (use >= 1 && !mbar_wait(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u)) {
+                const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
+                if (use >= 1 && !mbar_wait_or_abort(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u, abort_flag, true)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t dcol = tmem + (uint32_t)(buf * BN);
                 const int k0 = tm.kc0(z), k1 = tm.kc1(z);
-                for (int kc = k0; kc < k1; ++kc, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (uint32_t)(it / S) & 1u;
-                    if (!mbar_wait(&bars->full_b[s], ph) || !mbar_wait(&bars->full_a[s], ph) || *abort_flag) {
+                for (int kc = k0; kc < k1; ++kc) {
+                    if (!mbar_wait_or_abort(&bars->full_b[s], ph, abort_flag, true) ||
+                        !mbar_wait_or_abort(&bars->full_a[s], ph, abort_flag, true)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -288,6 +288,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                                     bdesc + (uint64_t)(2 * j), idesc, (kc > k0 || j > 0) ? 1u : 0u);
                     if (cl > 1) umma_commit_mc(&bars->empty[s], cmask);
                     else umma_commit(&bars->empty[s]);
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
                 umma_commit(&bars->acc_full[buf]);
             }
@@ -332,7 +333,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             ring[j] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
             if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
         }
-        int it = 0, slot = 0;
+        int it = 0, slot = 0, s = 0;
+        uint32_t ph = 0;                                   // ring slot and phase parity of item `it`
         bool ok = true;
         while (pr.t < tm.total && ok) {
             if ((it & 1) == h) {
@@ -344,9 +346,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                     ring[PF - 1] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
                     if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
                 }
-                const int s = it % S;
-                const uint32_t ph = (uint32_t)(it / S) & 1u;
-                if ((it >= S && !mbar_wait(&bars->empty[s], ph ^ 1u)) || *abort_flag) {
+                if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -362,6 +362,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             }
             step(pr);
             ++it;
+            if (++s == S) { s = 0; ph ^= 1u; }
             (void)slot;
         }
     } else if (warp >= 12) {                               // ---- epilogue
@@ -373,8 +374,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             int np, m, z;
             tm.decode(t, np, m, z);
             const int n = np * cl + rank;
-            const int buf = lt % NACC, use = lt / NACC;
-            if (!mbar_wait(&bars->acc_full[buf], (uint32_t)use & 1u) || *abort_flag) {
+            const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
+            if (!mbar_wait_or_abort(&bars->acc_full[buf], (uint32_t)use & 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;
             }

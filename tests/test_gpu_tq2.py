@@ -170,6 +170,60 @@ def test_gemv_grouped_64_jobs_bit_identical(lib):
         assert torch.equal(outs[i], single), i
 
 
+def _sampled_gemv_check(lib, N, K, Ms, wkey, xkey, nsample=400):
+    import torch
+    aos = synth.random_tq2(N, K, wkey)
+    w = lib.tq2_upload(aos, N, K)
+    codes, d_bits = otq2.parse_aos(aos, N, K)
+    rng = np.random.Generator(np.random.Philox(key=wkey + 7))
+    rows = sorted(set(rng.integers(0, N, nsample).tolist()) | set(range(8)) | set(range(N - 140, N)))
+    for M in Ms:
+        x = synth.random_x(M, K, xkey + M)
+        out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        lib.tq2_gemm(w, to_dev(x), out)
+        lib.device_status()
+        assert not torch.isnan(out).any().item()
+        got = out.cpu().numpy().astype(np.float64)
+        for m in range(M):
+            for n in rows:
+                ref, absref = otq2.gemm_elem(x[m], codes[n], d_bits[n])
+                err = abs(got[m, n] - ref)
+                assert err <= 1e-3 + 2e-4 * (K > 4096) and err <= 2.0 ** -12 * absref + 1e-7, (M, m, n, got[m, n], ref)
+
+
+def test_gemv_row_split_ragged(lib):
+    """Row-split GEMV with a ragged last unit (20000 = 156 x 128 + 32 rows)
+    and a partial last stage (K = 2176: 17 blocks)."""
+    _sampled_gemv_check(lib, 20000, 2176, (1, 2), 110, 111)
+
+
+def test_gemv_row_split_k8192(lib):
+    """Row-split GEMV at K = 8192, M = 1 and 2 (x held in shared memory)."""
+    _sampled_gemv_check(lib, 19600, 8192, (1, 2), 112, 113, nsample=200)
+
+
+def test_gemv_grouped_distinct_x(lib):
+    """A grouped call whose jobs each bring their own x: the row-split kernel
+    restages x at job boundaries inside a CTA's run of units."""
+    import torch
+    N, K = 4096, 1024
+    G = 40
+    aoss = [synth.random_tq2(N, K, 120 + i) for i in range(3)]
+    ws = [lib.tq2_upload(a, N, K) for a in aoss]
+    Ws = [otq2.dequant_aos(a, N, K) for a in aoss]
+    for M in (1, 2):
+        xs_np = [synth.random_x(M, K, 300 + 10 * M + g) for g in range(G)]
+        hs = [ws[g % 3] for g in range(G)]
+        outs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(G)]
+        lib.tq2_gemm_grouped(hs, [to_dev(x) for x in xs_np], outs)
+        lib.device_status()
+        for g in range(G):
+            x64 = np.asarray(xs_np[g], dtype=np.float64)
+            W = Ws[g % 3]
+            check_skinny(outs[g].cpu().numpy().astype(np.float64), x64 @ W.T, np.abs(x64) @ np.abs(W).T,
+                         f"M={M} job {g}")
+
+
 def test_gemv_mk_limit(lib):
     """M * K above the shared-memory limit of the fused GEMV: a single call
     falls back to the staged skinny kernel, a grouped call is refused."""
