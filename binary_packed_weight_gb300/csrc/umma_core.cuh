@@ -7,10 +7,10 @@
 // signs) decoded on chip; act is an f16 activation matrix staged in the K
 // order the decoder emits pairs in.  One CTA computes a 128 (plane rows) x BN
 // (tokens) tile:
-//   * eight decoder warps (one plane row per thread = its TMEM lane, two
-//     warps per lane quarter splitting each K stage) write the decoded f16
-//     pairs into tensor memory with tcgen05.st: the MMA's A operand never
-//     passes through shared memory;
+//   * eight decoder warps (one plane row per thread, two warps per row
+//     quarter taking alternate K stages) write the decoded f16 rows into a
+//     shared-memory ring in the MMA's K-major 128-byte-swizzled layout, so
+//     tensor memory holds only the two accumulators;
 //   * one thread issues TMA loads of the activation tile (B operand, 128-byte
 //     swizzle) into a 4-stage shared-memory ring;
 //   * one thread issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
@@ -30,6 +30,7 @@ constexpr int UM_BM = 128;       // plane rows per tile = MMA M
 constexpr int UM_BK = 64;        // K per pipeline stage (128 bytes of f16)
 constexpr int UM_STAGES = 8;     // ring slots allocated; the launch picks how many it uses
 constexpr int UM_MAX_BN = 256;   // MMA N limit for M = 128
+constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in shared memory (16 KB)
 // warp 0 TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 idle,
 // warps 4-11 decoders (two per TMEM lane quarter, taking alternate stages),
 // warps 12-15 epilogue (one per lane quarter)
@@ -190,7 +191,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_bytes = BN * 128;
-    UmmaBars* bars = reinterpret_cast<UmmaBars*>(smem + S * stage_bytes);
+    uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned
+    UmmaBars* bars = reinterpret_cast<UmmaBars*>(a_ring + S * UM_A_STAGE);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
     // tiles of the same unit and share its activation tile: each loads 1/cl
@@ -222,7 +224,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     if (cl > 1) cluster_sync();                          // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t a_col0 = (uint32_t)(NACC * BN);
     volatile int* abort_flag = &bars->abort;
 
     pdl_launch_dependents();
@@ -282,10 +283,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                     }
                     tc_fence_after();
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(a_ring + s * UM_A_STAGE));
 #pragma unroll
                     for (int j = 0; j < UM_BK / 16; ++j)
-                        umma_f16_ts(dcol, tmem + a_col0 + (uint32_t)(s * (UM_BK / 2) + j * 8),
-                                    bdesc + (uint64_t)(2 * j), idesc, (kc > k0 || j > 0) ? 1u : 0u);
+                        umma_f16_ss(dcol, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j), idesc,
+                                    (kc > k0 || j > 0) ? 1u : 0u);
                     if (cl > 1) umma_commit_mc(&bars->empty[s], cmask);
                     else umma_commit(&bars->empty[s]);
                     if (++s == S) { s = 0; ph ^= 1u; }
@@ -296,7 +298,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     } else if (warp >= 4 && warp < 12) {                   // ---- decoders
         // warp pair (q, h): lane quarter q, stages with item parity h
         const int q = warp & 3, h = (warp - 4) >> 2;
-        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        const int arow = q * 32 + lane;                    // row of the A stage this thread writes
         constexpr int PF = 3;                              // own items prefetched ahead
         // flattened walk over this CTA's (tile, kc) items, two cursors
         struct Cur {
@@ -351,12 +353,16 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 uint32_t v[32];
                 dec.decode(cur, v);
-                tmem_st_32x32b_x32(lane_addr + a_col0 + (uint32_t)(s * (UM_BK / 2)), v);
-                tmem_wait_st();
-                tc_fence_before();
+                // row arow of the stage: 16-byte chunk c (columns 4c..4c+3) at
+                // chunk c ^ (arow & 7), the layout TMA would write with 128-byte swizzle
+                uint8_t* rowp = a_ring + s * UM_A_STAGE + arow * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(rowp + ((c ^ (arow & 7)) << 4)) =
+                        make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                fence_proxy_async_shared();                // the MMA reads A through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->full_a[s]);
             }
@@ -454,20 +460,17 @@ cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, in
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
                             (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    // ring depth and accumulator count: two accumulators (epilogue overlaps
-    // the next tile) when they fit next to the A stages in 512 TMEM columns,
-    // else one; the B ring must also fit the shared memory.
-    int S, NACC;
-    if (2 * BN + 8 * (UM_BK / 2) <= 512) { S = 8; NACC = 2; }
-    else if (2 * BN + 4 * (UM_BK / 2) <= 512) { S = 4; NACC = 2; }
-    else { S = 6; NACC = 1; }
-    while (S > 2 && (size_t)S * BN * 128 + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
+    // two accumulators in tensor memory (the epilogue of a tile overlaps the
+    // next tile's MMAs); the A and B stage rings fill the shared memory
+    const int NACC = 2;
+    int S = UM_STAGES;
+    while (S > 2 && (size_t)S * (BN * 128 + UM_A_STAGE) + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
     int tmem_cols = 32;
-    while (tmem_cols < NACC * BN + S * (UM_BK / 2)) tmem_cols <<= 1;
+    while (tmem_cols < NACC * BN) tmem_cols <<= 1;
     // At least 120 KB of shared memory: no two CTAs of this kernel can share
     // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
     // (which a cluster barrier could otherwise turn into a deadlock).
-    size_t smem = (size_t)S * BN * 128 + 1024 + sizeof(UmmaBars) + 1024;
+    size_t smem = (size_t)S * (BN * 128 + UM_A_STAGE) + 1024 + sizeof(UmmaBars) + 1024;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
     tm.tiles_n = tiles_n;
