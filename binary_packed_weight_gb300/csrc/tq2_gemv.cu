@@ -332,13 +332,21 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
             mbar_arrive_expect_tx(&sfull[slot], sbytes);
             bulk_load(scb + slot * L.sc_bytes, J.scales + (int64_t)n0 * nb, sbytes, &sfull[slot]);
             if (++slot == sslots) { slot = 0; sph ^= 1u; }
-            for (int c = 0; c < nch; ++c, ++it) {
+            // row-split consumers take the pieces partial-major (c = j, j + 8,
+            // ... for j = 0..7); k-split consumers in order
+            for (int i = 0, c = 0, j = 0; i < nch; ++i, ++it) {
                 if (it >= stages) ok = mbar_wait(&empty[s], ph ^ 1u);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)GV_STAGE);
                 tma_load_3d(ring + s * GV_STAGE, &tab.job[job].map, &full[s], 0, n0,
                             MODE == GV_ROWS ? c : c * GV_CONS);
                 if (++s == stages) { s = 0; ph ^= 1u; }
+                if (MODE == GV_ROWS) {
+                    c += GV_CONS;
+                    if (c >= nch) c = ++j;
+                } else {
+                    ++c;
+                }
             }
         }
         return;
@@ -441,22 +449,17 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
         if (MODE == GV_KSPLIT) {
             for (int c = 0; c < nch; ++c) do_stage(c, totA, totB);
         } else {
-            // Eight partial sums, one per piece index mod 8: the blocks of
-            // partial j are exactly those warp j owns in a k-split launch,
-            // taken in the same order, and the partials are added in the
-            // same order as the k-split reduction.
-            float pa[GV_CONS], pb[GV_CONS];
-#pragma unroll
-            for (int j = 0; j < GV_CONS; ++j) pa[j] = pb[j] = 0.f;
-            for (int c0 = 0; c0 < nch; c0 += GV_CONS) {
-#pragma unroll
-                for (int j = 0; j < GV_CONS; ++j)
-                    if (c0 + j < nch) do_stage(c0 + j, pa[j], pb[j]);
-            }
-#pragma unroll
+            // Eight partial sums, one per piece index mod 8, taken one after
+            // the other (the producer loads the pieces in this order): the
+            // blocks of partial j are exactly those warp j owns in a k-split
+            // launch, in the same order, and the partials are added in the
+            // same order as the k-split reduction.  One partial pair is live
+            // at a time instead of eight.
             for (int j = 0; j < GV_CONS; ++j) {
-                totA += pa[j];
-                totB += pb[j];
+                float pa = 0.f, pb = 0.f;
+                for (int c = j; c < nch; c += GV_CONS) do_stage(c, pa, pb);
+                totA += pa;
+                totB += pb;
             }
         }
         __syncwarp();
