@@ -59,22 +59,24 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
-def src_hash():
+def src_hash(files):
+    """Hash of the kernel sources `files` (names under csrc/, in order)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "binary_packed_weight_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(key):
-    """DRAM bytes per launch from the committed ncu summary, if the kernels
-    have not changed since it was taken (else None)."""
+    """DRAM bytes per launch from the committed ncu summary, if the sources
+    the kernel is compiled from have not changed since it was taken (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path)).get(key)
-    if not d or d.get("src_hash") != src_hash():
+    if not d or not d.get("sources") or d.get("src_hash") != src_hash(d["sources"]):
         return None
     return d.get("dram_bytes")
 

@@ -32,7 +32,7 @@ constexpr int UM_STAGES = 8;     // ring slots allocated; the launch picks how m
 constexpr int UM_MAX_BN = 256;   // MMA N limit for M = 128
 constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in shared memory (16 KB)
 // warp 0 TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 idle,
-// warps 4-11 decoders (two per TMEM lane quarter, taking alternate stages),
+// warps 4-11 decoders (two per 32-row quarter of the tile, taking alternate stages),
 // warps 12-15 epilogue (one per lane quarter)
 constexpr int UM_THREADS = 512;
 
@@ -61,8 +61,9 @@ __device__ __forceinline__ uint2 ldg_u2_nc(const void* p) {
 
 // ---------------------------------------------------------------- decoders ----
 // A decoder turns K-stage kc (64 elements) of plane row `row` (valid iff ok)
-// into 32 f16 pairs v[0..31]: TMEM column j of the stage holds K positions
-// 2j, 2j+1 of the permuted order the activations are staged in.  Loads go
+// into 32 f16 pairs v[0..31]: pair j of the row holds K positions 2j, 2j+1 of
+// the permuted order the activations are staged in (16-byte chunk j/4 of the
+// row's 128 bytes, before the swizzle).  Loads go
 // through L1 (the neighbouring stage of the same 32-byte sector is read by
 // the partner decoder warp).
 
