@@ -305,6 +305,23 @@ def extra_large(torch, bpw, stream, dev, pk):
                 bound="tensor", includes="x f32->f16 staging kernel + GEMM")
 
 
+def extra_quantize(torch, bpw, stream, dev, pk):
+    """The ternary producer at the large GEMM's weight shape: f32 [N][K] in,
+    BlockTQ2_0_g128 blocks out (inputs larger than L2)."""
+    cfg = synth.LARGE
+    N, K = cfg["N"], cfg["K"]
+    W = torch.from_numpy(synth.random_weights_f32(N, K, cfg["wkey"] + 40)).to(dev)
+    aos = torch.empty(N * (K // 128) * 34, dtype=torch.uint8, device=dev)
+
+    def step():
+        bpw.tq2_quantize(W, aos, stream=stream.cuda_stream)
+    secs, _ = time_graph(torch, step, 20, 3, stream)
+    t = secs / 20
+    nbytes = N * K * 4 + N * (K // 128) * 34
+    return dict(us=t * 1e6, alg_gbs=nbytes / t / 1e9, hbm_frac=nbytes / t / 1e9 / pk["hbm"], bound="hbm",
+                algorithmic_bytes=nbytes, workload=f"f32 W [{N}][{K}] -> BlockTQ2_0_g128")
+
+
 # ------------------------------------------------------------ cpu oracle ----
 def oracle_gemv_sample(budget_s=12.0):
     """The f64 oracle on the GEMV workload, repeated for about budget_s seconds."""
@@ -405,6 +422,8 @@ def main():
             extra["tq2_large_M4096_N14336"] = extra_large(torch, bpw, stream, dev, pk)
         if not only or "blr" in only:
             extra["blr_T2048_d4096_r512"] = extra_blr(torch, bpw, stream, dev, pk)
+        if not only or "quantize" in only:
+            extra["tq2_quantize_N14336_K4096"] = extra_quantize(torch, bpw, stream, dev, pk)
 
     if rank != 0:
         return

@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
-    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "blr_expand_bits", "blr_forward", "blr_backward",
+    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward",
     "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -38,6 +38,7 @@ _SIGS = {
     "tq2_gemm_grouped": (_I, [_P, _P, _P, _I, _I64, _I64, _P]),
     "tq2_unpack": (_I, [_P, _P, _P]),
     "tq2_dequant_f16": (_I, [_P, _P, _P]),
+    "tq2_quantize": (_I, [_P, _I64, _I64, _P, _P]),
     "blr_expand_bits": (_I, [_P, _I64, _I64, _P, _I, _P]),
     "blr_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "blr_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -158,6 +159,14 @@ def tq2_unpack(w, stream=None):
 def tq2_dequant_f16(w, out_u16, stream=None):
     _check(load().tq2_dequant_f16(w.handle, _ptr(out_u16), _stream(stream)), "tq2_dequant_f16")
     return out_u16
+
+
+def tq2_quantize(w, aos_out, stream=None):
+    """f32 weights ``w`` [N, K] (device) -> BlockTQ2_0_g128 blocks in ``aos_out``
+    (device uint8, N*(K/128)*34 bytes)."""
+    N, K = w.shape
+    _check(load().tq2_quantize(_ptr(w), N, K, _ptr(aos_out), _stream(stream)), "tq2_quantize")
+    return aos_out
 
 
 def blr_expand_bits(bits, rows, r, plane, transpose, stream=None):

@@ -262,6 +262,17 @@ tq2_status tq2_unpack(tq2_handle h, void* aos_out, void* stream) {
     return TQ2_OK;
 }
 
+tq2_status tq2_quantize(const float* w, int64_t N, int64_t K, void* aos_out, void* stream) {
+    if (!w || !aos_out) return fail(TQ2_EINVAL, "tq2_quantize: null pointer");
+    if (N < 1 || K < 128 || K % 128 != 0)
+        return fail(TQ2_ESHAPE, "tq2_quantize: need N >= 1, K >= 128, K %% 128 == 0 (N=%lld K=%lld)", (long long)N,
+                    (long long)K);
+    if (N > ((int64_t)1 << 40) / K) return fail(TQ2_ESHAPE, "tq2_quantize: weight too large");
+    cudaError_t e = tq2::launch_quantize(w, static_cast<uint8_t*>(aos_out), N, K, S(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq2_quantize");
+    return TQ2_OK;
+}
+
 tq2_status tq2_dequant_f16(tq2_handle h, uint16_t* w, void* stream) {
     if (!h || !w) return fail(TQ2_EINVAL, "tq2_dequant_f16: null pointer");
     cudaError_t e = tq2::launch_dequant_f16(h->codes, h->scales, w, h->N, h->K, S(stream));

@@ -177,6 +177,28 @@ TQ2_API tq2_status tq2_unpack(tq2_handle h, void* aos_out, void* stream);
 TQ2_API tq2_status tq2_dequant_f16(tq2_handle h, uint16_t* w, void* stream);
 
 /*
+ * tq2_quantize -- the ternary producer: f32 weights -> BlockTQ2_0_g128 blocks.
+ * Passage: the 2-bit FakeQuantize helpers of "rlx-mlx 0.2.13,
+ * src/lower/helpers.rs" (fq_q_max gives q_max = 1 for 2 bits; the scale is
+ * max|w| / q_max floored at 1e-12; the value is round(w / scale) clamped to
+ * [-q_max, q_max]), applied per 128-element block of a row in f32:
+ *   s = max(max|w|, 1e-12);  q = clamp(round_half_even(w / s), -1, 1);
+ *   code = q + 1;  d = f16(s), nearest with ties to even.
+ * The block granularity and the half-to-even rounding are readings: the page
+ * reduces per channel or per tensor and stores no codes.
+ *
+ *   w        DEVICE float32[N][K], row-major, finite values (NaN or Inf give
+ *            unspecified codes).  Read only.
+ *   N, K     N >= 1, K >= 128, K % 128 == 0, N*K < 2^40.  Else TQ2_ESHAPE.
+ *   aos_out  DEVICE, N*(K/128) blocks of 34 bytes in the tq2_upload layout
+ *            (block kb of row n at index n*(K/128)+kb), overwritten.  Copy
+ *            it to the host and pass it to tq2_upload to use the weights.
+ *   stream   the launch is asynchronous on it.
+ * Null pointers: TQ2_EINVAL.
+ */
+TQ2_API tq2_status tq2_quantize(const float* w, int64_t N, int64_t K, void* aos_out, void* stream);
+
+/*
  * tq2_gemm_skinny_static -- the skinny GEMM (M <= 16) without any device
  * allocation.  The pages have no counterpart to this call; it exists for
  * callers that must not allocate while they run a GEMM: plugin or custom-op

@@ -88,3 +88,50 @@ def gemm_elem(x_row, codes_row, d_row):
     w = (codes_row.astype(np.float64) - 1.0) * np.repeat(f16.bits_to_float(d_row), BLOCK_K)
     xr = np.asarray(x_row, dtype=np.float64)
     return float(np.dot(xr, w)), float(np.dot(np.abs(xr), np.abs(w)))
+
+
+def pack_aos(codes, d_bits):
+    """Codes ``uint8 [N][K]`` and scale bits ``uint16 [N][K/128]`` -> AoS bytes.
+
+    The inverse of :func:`parse_aos`: code of element ``4*j + i`` of a block
+    in bits ``2i, 2i+1`` of byte ``j``, then ``d`` little-endian.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    nb = K // BLOCK_K
+    c = codes.reshape(N * nb, QS_BYTES, 4)
+    qs = c[:, :, 0] | (c[:, :, 1] << 2) | (c[:, :, 2] << 4) | (c[:, :, 3] << 6)
+    d = np.asarray(d_bits, dtype=np.uint16).reshape(N * nb, 1)
+    out = np.concatenate([qs.astype(np.uint8), (d & 0xFF).astype(np.uint8), (d >> 8).astype(np.uint8)], axis=1)
+    return out.tobytes()
+
+
+def quantize(W):
+    """f32 weights ``[N][K]`` -> ternary codes ``uint8 [N][K]`` and f16 scale bits ``uint16 [N][K/128]``.
+
+    Source: "rlx-mlx 0.2.13, src/lower/helpers.rs", the FakeQuantize helpers
+    (``fq_q_max``, ``fq_scale_perbatch``, ``fq_quantize_dequantize``).  For 2
+    bits ``q_max = 1``; the scale is ``max|w| / q_max`` floored at ``1e-12``;
+    the quantized value is ``round(w / scale)`` clamped to ``[-q_max, q_max]``
+    (the page then multiplies back by the scale).  Everything runs in the
+    arrays' dtype, f32.
+
+    Readings (the page reduces per channel or per tensor and stores nothing):
+      * the maximum is taken over each 128-element block of a row, the
+        granularity of ``BlockTQ2_0_g128``;
+      * ``round`` rounds half to even, as the page's array library does;
+      * the stored code is ``q + 1`` and ``d`` is the f32 scale rounded to
+        f16 (nearest, ties to even).
+    """
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    if K % BLOCK_K:
+        raise ValueError("K must be a multiple of 128")
+    blocks = W.reshape(N, K // BLOCK_K, BLOCK_K)
+    q_max = np.float32(1.0)
+    scale = np.maximum(np.abs(blocks).max(axis=2, keepdims=True) / q_max, np.float32(1e-12))
+    q = np.clip(np.rint(blocks / scale), -q_max, q_max)
+    codes = (q + np.float32(1.0)).astype(np.uint8).reshape(N, K)
+    with np.errstate(over="ignore"):                  # scales above the f16 range round to +inf
+        d_bits = f16.round_to_f16_bits(scale[..., 0].astype(np.float64)).astype(np.uint16)
+    return codes, d_bits

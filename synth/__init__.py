@@ -177,6 +177,15 @@ def random_x(M, K, key):
     return normal(M * K, key).reshape(M, K)
 
 
+def random_weights_f32(N, K, key):
+    """Dense f32 weights ``[N][K]`` for the ternary producer: iid N(0, 1)
+    times a per-row magnitude drawn log-uniformly from [1e-3, 1e3], so that
+    block maxima span six decades."""
+    w = normal(N * K, key).reshape(N, K)
+    mag = np.exp(uniform(N, key + 1, np.log(1e-3), np.log(1e3))).astype(np.float32)
+    return (w * mag[:, None]).astype(np.float32)
+
+
 def blr_inputs(T, d_in, d_out, r, key):
     """One blr path: bitmaps, metric vectors and x, dy (all iid, see module doc)."""
     return dict(

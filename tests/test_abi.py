@@ -23,7 +23,7 @@ def cdll():
 
 def test_header_declares_the_boundary():
     names = set(_declared())
-    for want in ("tq2_upload", "tq2_free", "tq2_gemm", "tq2_unpack", "tq2_dequant_f16",
+    for want in ("tq2_upload", "tq2_free", "tq2_gemm", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize",
                  "blr_expand_bits", "blr_forward", "blr_backward"):
         assert want in names
 

@@ -390,3 +390,81 @@ def test_edge_cases(lib):
             else:
                 (check_skinny(got, r[0], r[1]) if M <= 16 else check_tensor(got, *r))
     lib.device_status()
+
+
+# ---- ternary producer (f32 weights -> BlockTQ2_0_g128), bit-exact against the oracle
+
+def _quantize_gpu(lib, W):
+    import torch
+    N, K = W.shape
+    aos = torch.zeros(N * (K // 128) * 34, dtype=torch.uint8, device="cuda")
+    lib.tq2_quantize(to_dev(W), aos)
+    lib.device_status()
+    return aos.cpu().numpy().tobytes()
+
+
+@pytest.mark.gpu
+def test_quantize_matches_oracle_with_edge_blocks(lib):
+    N, K = 300, 640
+    W = synth.random_weights_f32(N, K, 301)
+    blocks = W.reshape(N, K // 128, 128)
+    blocks[3, 2, :] = 0.0                                   # all-zero block: codes 1, d = f16(1e-12) = 0
+    m = np.abs(blocks[5, 1]).max()
+    blocks[5, 1, 7], blocks[5, 1, 9] = 0.5 * m, -0.5 * m    # exact ties: round half to even -> 0
+    blocks[6, 0, :] = -1.0                                  # every weight at the (negative) maximum
+    blocks[7, 4, :] = 1e-30                                 # tiny values (f16(scale) underflows to 0)
+    blocks[8, 3, 100] = 1e30                                # one huge value (f16(scale) overflows to inf)
+    W = blocks.reshape(N, K)
+    got = _quantize_gpu(lib, W)
+    want = otq2.pack_aos(*otq2.quantize(W))
+    assert got == want
+
+
+@pytest.mark.gpu
+def test_quantize_full_size_and_shapes(lib):
+    for N, K in ((1, 128), (14336, 4096)):
+        W = synth.random_weights_f32(N, K, 302 + N)
+        assert _quantize_gpu(lib, W) == otq2.pack_aos(*otq2.quantize(W)), (N, K)
+    import torch
+    with pytest.raises(lib.TQ2Error):
+        lib.tq2_quantize(torch.zeros((4, 200), device="cuda"), torch.zeros(1000, dtype=torch.uint8, device="cuda"))
+
+
+@pytest.mark.gpu
+def test_quantized_weights_feed_the_gemm(lib):
+    """Producer -> tq2_upload -> GEMM, against the oracle on the oracle's codes.
+    Weights N(0, 0.03^2), so block scales fall near the pages' U(0.01, 0.1)
+    and the pages' absolute bound applies."""
+    N, K = 1000, 1024
+    W = (synth.random_x(N, K, 303) * np.float32(0.03)).astype(np.float32)
+    aos = _quantize_gpu(lib, W)
+    w = lib.tq2_upload(aos, N, K)
+    for M in (1, 8, 64):
+        x = synth.random_x(M, K, 304 + M)
+        got = run_gemm(lib, w, x)
+        ref, absref, ref16, absref16 = oracle_gemm(aos, N, K, x)
+        (check_skinny(got, ref, absref, f"quantized M={M}") if M <= 16 else check_tensor(got, ref, absref, ref16, absref16, f"quantized M={M}"))
+
+
+@pytest.mark.gpu
+def test_quantize_quotients_next_to_one_half(lib):
+    """Weights whose quotient w / s rounds to just below, exactly at, or just
+    above +-0.5 in f32, for scales that are not powers of two: the producer's
+    rounding decision must be the one of the correctly rounded division."""
+    rows = []
+    for s in (3.0, 5.0, 7.0, 0.3, 1.7e-5, 6e4):
+        s = np.float32(s)
+        h = np.float32(0.5) * s
+        vals = [s]                                     # the block maximum
+        w = h
+        for _ in range(20):                            # floats walking up from s/2
+            vals += [w, -w]
+            w = np.nextafter(w, np.float32(np.inf))
+        w = h
+        for _ in range(20):                            # and down
+            w = np.nextafter(w, np.float32(0))
+            vals += [w, -w]
+        vals = np.array(vals[:128] + [0.0] * (128 - min(len(vals), 128)), dtype=np.float32)
+        rows.append(vals)
+    W = np.stack(rows).astype(np.float32)
+    assert _quantize_gpu(lib, W) == otq2.pack_aos(*otq2.quantize(W))

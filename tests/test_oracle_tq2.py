@@ -153,3 +153,79 @@ def test_rejects_bad_shapes():
 def test_vectorised_lcg_equals_the_page_loop():
     for seed in (0x12345678, 0xDEADBEEF ^ 3072, 0x9E3779B1 ^ (40 << 8) ^ 256):
         assert np.array_equal(synth.lcg_codes(5000, seed), synth.lcg_codes_loop(5000, seed))
+
+
+# ---- ternary producer ("rlx-mlx 0.2.13, src/lower/helpers.rs", FakeQuantize helpers, 2 bits)
+
+def _random_codes_scales(N, K, seed):
+    """Codes in {0,1,2} with at least one nonzero weight (code 0 or 2) per block,
+    and positive normal f16 scales."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 3, size=(N, K)).astype(np.uint8)
+    codes.reshape(N, K // 128, 128)[:, :, 0] = rng.choice([0, 2], size=(N, K // 128))
+    d = rng.uniform(0.01, 0.1, size=(N, K // 128))
+    return codes, tq2.f16.round_to_f16_bits(d).astype(np.uint16)
+
+
+def test_quantize_inverts_dequant():
+    # W = (c - 1) * d exactly in f32; the block maximum is d, so w / d = c - 1
+    # exactly and the producer must return the same codes and scales
+    codes, d_bits = _random_codes_scales(7, 512, 11)
+    W = tq2.dequant(codes, d_bits).astype(np.float32)
+    c2, d2 = tq2.quantize(W)
+    assert np.array_equal(c2, codes)
+    assert np.array_equal(d2, d_bits)
+    assert tq2.pack_aos(c2, d2) == tq2.pack_aos(codes, d_bits)
+
+
+def test_quantize_ties_round_half_to_even():
+    w = np.zeros((1, 128), dtype=np.float32)
+    w[0, 0] = 1.0                                  # block maximum: scale 1
+    w[0, 1], w[0, 2] = 0.5, -0.5                   # ties -> 0 (even), not +-1
+    w[0, 3], w[0, 4] = np.nextafter(np.float32(0.5), np.float32(1)), np.nextafter(np.float32(-0.5), np.float32(-1))
+    w[0, 5], w[0, 6] = np.nextafter(np.float32(0.5), np.float32(0)), -1.0
+    codes, d_bits = tq2.quantize(w)
+    assert list(codes[0, :7]) == [2, 1, 1, 2, 0, 1, 0]
+    assert int(d_bits[0, 0]) == 0x3C00             # f16 1.0
+
+
+def test_quantize_zero_block_and_floor():
+    # max|w| = 0: the 1e-12 floor keeps the division finite; f16(1e-12) is 0
+    codes, d_bits = tq2.quantize(np.zeros((2, 256), dtype=np.float32))
+    assert np.all(codes == 1) and np.all(d_bits == 0)
+
+
+def test_quantize_scale_per_block_not_per_row():
+    w = np.zeros((1, 256), dtype=np.float32)
+    w[0, :128] = np.linspace(-2.0, 2.0, 128, dtype=np.float32)      # block 0: max 2
+    w[0, 128:] = np.linspace(-0.25, 0.25, 128, dtype=np.float32)    # block 1: max 0.25
+    codes, d_bits = tq2.quantize(w)
+    assert int(d_bits[0, 0]) == 0x4000 and int(d_bits[0, 1]) == 0x3400   # f16 2.0, 0.25
+    # each block uses its own maximum: the same relative pattern gives the same codes
+    assert np.array_equal(codes[0, :128], codes[0, 128:])
+    assert codes[0, 0] == 0 and codes[0, 127] == 2 and codes[0, 64] == 1
+
+
+def test_quantize_error_and_sign_bounds():
+    rng = np.random.default_rng(5)
+    W = (rng.standard_normal((9, 640)) * rng.uniform(0.01, 10, size=(9, 1))).astype(np.float32)
+    codes, d_bits = tq2.quantize(W)
+    Wq = tq2.dequant(codes, d_bits)
+    blocks = np.abs(W.reshape(9, 5, 128)).max(axis=2)                       # the f32 scales
+    d = tq2.f16.bits_to_float(d_bits)
+    bound = np.repeat(np.abs(d - blocks) + blocks / 2, 128, axis=1)          # |q(d - s)| + s/2
+    assert np.all(np.abs(Wq - W) <= bound * (1 + 1e-6))
+    q = codes.astype(np.int64) - 1
+    assert np.all(q * np.sign(W) >= 0)                                       # never the opposite sign
+
+
+def test_quantize_scale_outside_the_f16_range():
+    w = np.zeros((1, 256), dtype=np.float32)
+    w[0, 5] = 1e5                          # above the f16 maximum 65504: d rounds to +inf
+    w[0, 128 + 9] = -3e-8                  # f16 subnormal range: d = 3e-8 rounds to 2^-25 -> 0x0000 or 0x0001
+    codes, d_bits = tq2.quantize(w)
+    assert int(d_bits[0, 0]) == 0x7C00
+    assert codes[0, 5] == 2 and codes[0, 128 + 9] == 0
+    assert int(d_bits[0, 1]) == 0x0000 or int(d_bits[0, 1]) == 0x0001
+    # 3e-8 lies between 2^-25 (the midpoint of 0 and the smallest subnormal 2^-24) and 2^-24: rounds up
+    assert int(d_bits[0, 1]) == 0x0001
