@@ -8,6 +8,7 @@
 
 #include "../../include/tq2.h"
 #include "tq2_internal.h"
+#include "tq2_quant.h"
 
 namespace {
 

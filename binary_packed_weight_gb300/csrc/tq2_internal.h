@@ -63,9 +63,6 @@ cudaError_t launch_gemv(const tq2_weight* const* ws, const float* const* xs, flo
                         cudaStream_t st);
 unsigned int read_clear_dev_error_gemv(cudaStream_t st);
 
-// tq2_quant.cu: f32 weights -> BlockTQ2_0_g128 AoS blocks (device to device).
-cudaError_t launch_quantize(const float* w, uint8_t* aos, int64_t N, int64_t K, cudaStream_t st);
-
 // tq2_umma.cu
 size_t tensor_scratch_bytes(int64_t M, int64_t K);
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,

@@ -20,6 +20,7 @@
 
 #include "ptx.cuh"
 #include "tq2_internal.h"
+#include "tq2_quant.h"
 
 namespace tq2 {
 
