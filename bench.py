@@ -305,6 +305,27 @@ def extra_large(torch, bpw, stream, dev, pk):
                 bound="tensor", includes="x f32->f16 staging kernel + GEMM")
 
 
+def extra_dit(torch, bpw, stream, dev, pk):
+    """The pages' two DiT shapes on the large-M tensor path (M=1536, K=3072)."""
+    res = {}
+    for cfg in synth.DIT:
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        w = bpw.tq2_upload(synth.random_tq2(N, K, cfg["wkey"]), N, K)
+        x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def step():
+            bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
+        secs, _ = time_graph(torch, step, 10, 3, stream)
+        t = secs / 10
+        tfl = 2.0 * M * N * K / t / 1e12
+        w.free()
+        res[f"M{M}_N{N}_K{K}"] = dict(us=t * 1e6, tflops=tfl, tensor_frac=tfl / pk["bf16"],
+                                      tensor_frac_sustained=tfl / pk["bf16_sus"] if pk.get("bf16_sus") else None,
+                                      bound="tensor", includes="x f32->f16 staging kernel + GEMM")
+    return res
+
+
 def extra_quantize(torch, bpw, stream, dev, pk):
     """The ternary producer at the large GEMM's weight shape: f32 [N][K] in,
     BlockTQ2_0_g128 blocks out (inputs larger than L2)."""
@@ -422,6 +443,8 @@ def main():
             extra["tq2_large_M4096_N14336"] = extra_large(torch, bpw, stream, dev, pk)
         if not only or "blr" in only:
             extra["blr_T2048_d4096_r512"] = extra_blr(torch, bpw, stream, dev, pk)
+        if not only or "dit" in only:
+            extra["tq2_dit_M1536_K3072"] = extra_dit(torch, bpw, stream, dev, pk)
         if not only or "quantize" in only:
             extra["tq2_quantize_N14336_K4096"] = extra_quantize(torch, bpw, stream, dev, pk)
 

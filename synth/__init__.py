@@ -203,4 +203,8 @@ def blr_inputs(T, d_in, d_out, r, key):
 GEMV = dict(name="tq2_gemv", M=1, N=4096, K=4096, wkey=2, xkey=4)
 SKINNY = dict(name="tq2_skinny", Ms=(8, 32, 128), N=11008, K=4096, wkey=5, xkey=7)
 LARGE = dict(name="tq2_large", M=4096, N=14336, K=4096, wkey=8, xkey=10)
+# the two DiT shapes of the pages' Metal benchmark ("oxibonsai-kernels 0.2.1", bench over
+# (M, N, K) = (1536, 27648, 3072) and (1536, 3072, 3072)), same distributions as LARGE
+DIT = (dict(name="tq2_dit_wide", M=1536, N=27648, K=3072, wkey=20, xkey=21),
+       dict(name="tq2_dit_square", M=1536, N=3072, K=3072, wkey=22, xkey=23))
 BLR = dict(name="blr_layer", T=2048, d_in=4096, d_out=4096, r=512, key=11)

@@ -320,8 +320,18 @@ def test_tensor_large_sampled(lib):
     """M=4096, N=14336, K=4096 in the benchmarked launch configuration; the
     oracle computes sampled outputs one by one (random elements plus two full
     rows and two full columns)."""
+    _tensor_sampled(lib, synth.LARGE)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", synth.DIT, ids=[c["name"] for c in synth.DIT])
+def test_tensor_dit_shapes_sampled(lib, cfg):
+    """The pages' two DiT shapes, M=1536 and K=3072 with N=27648 or 3072."""
+    _tensor_sampled(lib, cfg)
+
+
+def _tensor_sampled(lib, cfg):
     import torch
-    cfg = synth.LARGE
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     aos = synth.random_tq2(N, K, cfg["wkey"])
     w = lib.tq2_upload(aos, N, K)
