@@ -478,3 +478,15 @@ def test_quantize_quotients_next_to_one_half(lib):
         rows.append(vals)
     W = np.stack(rows).astype(np.float32)
     assert _quantize_gpu(lib, W) == otq2.pack_aos(*otq2.quantize(W))
+
+
+@pytest.mark.gpu
+def test_tiny_page_against_golden(tiny, lib):
+    """The GPU on the page's tiny data against the stored oracle outputs
+    (tests/golden/tq2_page_tiny_M*.txt), within the pages' 1e-3 bound."""
+    from test_golden import load_matrix
+    aos, N, K, xs, w = tiny
+    for M in (1, 7):
+        got = run_gemm(lib, w, xs[M])
+        want = load_matrix(f"tq2_page_tiny_M{M}.txt")
+        assert np.abs(got - want).max() <= 1e-3, M
