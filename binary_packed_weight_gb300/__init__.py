@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
-    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward",
+    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths",
     "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -43,7 +43,15 @@ _SIGS = {
     "blr_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "blr_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                           _I64, _I64, _I64, _I64, _F, _P]),
+    "blr_forward_paths": (_I, [_P, _I, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "blr_backward_paths": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _P]),
 }
+
+
+class BlrPath(ctypes.Structure):
+    """``blr_path`` of include/tq2.h: device pointers of one path."""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("bits_u", "bits_v", "h", "l", "g", "a_save", "c_save", "dh", "dl", "dg")]
 
 
 class TQ2Error(RuntimeError):
@@ -189,6 +197,34 @@ def blr_backward(bits_u, bits_v, h, l, g, x, dy, a_save, c_save, dx, dh, dl, dg,
     _check(load().blr_backward(_ptr(bits_u), _ptr(bits_v), _ptr(h), _ptr(l), _ptr(g), _ptr(x), _ptr(dy),
                                _ptr(a_save), _ptr(c_save), _ptr(dx), _ptr(dh), _ptr(dl), _ptr(dg),
                                T, d_in, d_out, r, float(gscale), _stream(stream)), "blr_backward")
+    return dx
+
+
+def _paths_array(paths):
+    """List of dicts of tensors (keys as BlrPath's fields; missing ones are NULL)."""
+    arr = (BlrPath * len(paths))()
+    for i, p in enumerate(paths):
+        for name, _ in BlrPath._fields_:
+            setattr(arr[i], name, _ptr(p.get(name)))
+    return arr
+
+
+def blr_forward_paths(paths, x, y, stream=None):
+    """y = sum over paths, combined with the pages' rounding (see include/tq2.h)."""
+    T, d_in = x.shape
+    d_out, r = paths[0]["h"].numel(), paths[0]["l"].numel()
+    arr = _paths_array(paths)
+    _check(load().blr_forward_paths(ctypes.cast(arr, _P), len(paths), _ptr(x), _ptr(y), T, d_in, d_out, r,
+                                    _stream(stream)), "blr_forward_paths")
+    return y
+
+
+def blr_backward_paths(paths, x, dy, dx, gscale=1.0, stream=None):
+    T, d_in = x.shape
+    d_out, r = paths[0]["h"].numel(), paths[0]["l"].numel()
+    arr = _paths_array(paths)
+    _check(load().blr_backward_paths(ctypes.cast(arr, _P), len(paths), _ptr(x), _ptr(dy), _ptr(dx), T, d_in, d_out,
+                                     r, float(gscale), _stream(stream)), "blr_backward_paths")
     return dx
 
 

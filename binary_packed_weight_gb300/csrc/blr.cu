@@ -303,22 +303,21 @@ tq2_status blr_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, uint16
                        "blr_expand_bits");
 }
 
-tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
-                       const float* x, float* y, float* a_save, float* c_save, int64_t T, int64_t d_in, int64_t d_out,
-                       int64_t r, void* stream) {
-    if (!bits_u || !bits_v || !h || !l || !g || !x || !y || !a_save)
-        return blr_fail(TQ2_EINVAL, "blr_forward: null pointer");
-    tq2_status s = check_shapes("blr_forward", T, d_in, d_out, r);
-    if (s != TQ2_OK) return s;
-    if (!aligned16(x) || !aligned16(g) || !aligned16(l))
-        return blr_fail(TQ2_EINVAL, "blr_forward: x, g and l must be 16-byte aligned");
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// One path forward; accumulate: y = fl(y + fl(h.c)) instead of y = fl(h.c).
+// Arguments already checked.
+tq2_status forward_one(const char* who, const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l,
+                       const float* g, const float* x, float* y, float* a_save, float* c_save, int64_t T, int64_t d_in,
+                       int64_t d_out, int64_t r, int accumulate, cudaStream_t st) {
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
     const size_t bytes = (size_t)r * d_in / 8 + 256 + (size_t)T * d_in * 2 + 256 + (size_t)T * r * 2 + 256 +
                          (size_t)8 * T * r * 4 + 256;
     void* mem = nullptr;
     cudaError_t e = cudaMallocAsync(&mem, bytes, st);
-    if (e != cudaSuccess) return cuda_status(e, "blr_forward: scratch");
+    if (e != cudaSuccess) return cuda_status(e, who);
     Scratch sc{reinterpret_cast<char*>(mem), 0};
     uint32_t* bits_vT = sc.take<uint32_t>((size_t)r * d_in / 32);
     void* al16 = sc.take<uint16_t>((size_t)T * r);
@@ -326,28 +325,20 @@ tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, const flo
     if (e == cudaSuccess) e = forward_a(bits_vT, x, g, l, a_save, al16, iT, din, ir, sc, st);
     if (e == cudaSuccess) {
         DecSign dec{bits_u, (int64_t)r / 32};
-        EpiArgs ep{y, c_save, h, nullptr, nullptr, (int64_t)d_out, 1.0f};
+        EpiArgs ep{y, c_save, h, nullptr, nullptr, (int64_t)d_out, 1.0f, accumulate};
         e = launch_umma<DecSign, EPI_SCALE>(dec, ep, al16, iT, dout, ir, umma_pick_bn(iT), 1, st);
     }
     cudaError_t e2 = cudaFreeAsync(mem, st);
-    if (e != cudaSuccess) return cuda_status(e, "blr_forward");
-    return cuda_status(e2, "blr_forward: scratch free");
+    if (e != cudaSuccess) return cuda_status(e, who);
+    return cuda_status(e2, who);
 }
 
-tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
-                        const float* x, const float* dy, const float* a_save, const float* c_save, float* dx, float* dh,
-                        float* dl, float* dg, int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale,
-                        void* stream) {
-    if (!bits_u || !bits_v || !h || !l || !g || !x || !dy || !a_save || !dx || !dh || !dl || !dg)
-        return blr_fail(TQ2_EINVAL, "blr_backward: null pointer");
-    tq2_status s = check_shapes("blr_backward", T, d_in, d_out, r);
-    if (s != TQ2_OK) return s;
-    int ex = 0;
-    if (!(gscale > 0.f) || !std::isfinite(gscale) || std::frexp(gscale, &ex) != 0.5f)
-        return blr_fail(TQ2_EINVAL, "blr_backward: gscale must be a positive power of two");
-    if (!aligned16(dy) || !aligned16(h) || !aligned16(l) || !aligned16(a_save))
-        return blr_fail(TQ2_EINVAL, "blr_backward: dy, h, l and a_save must be 16-byte aligned");
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+// One path backward; accumulate: dx = fl(dx + fl(g.dx')) instead of fl(g.dx').
+// Arguments already checked.
+tq2_status backward_one(const char* who, const uint32_t* bits_u, const uint32_t* bits_v, const float* h,
+                        const float* l, const float* g, const float* x, const float* dy, const float* a_save,
+                        const float* c_save, float* dx, float* dh, float* dl, float* dg, int64_t T, int64_t d_in,
+                        int64_t d_out, int64_t r, float gscale, int accumulate, cudaStream_t st) {
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
     const int BN = umma_pick_bn(iT);
     const int ttiles = (iT + BN - 1) / BN, chunks = (iT + FIN_TC - 1) / FIN_TC;
@@ -356,7 +347,7 @@ tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const fl
                          (size_t)8 * T * r * 4 + 256 + (size_t)(ttiles + chunks + 2) * (mx + r) * 4 * 2 + 1024;
     void* mem = nullptr;
     cudaError_t e = cudaMallocAsync(&mem, bytes, st);
-    if (e != cudaSuccess) return cuda_status(e, "blr_backward: scratch");
+    if (e != cudaSuccess) return cuda_status(e, who);
     Scratch sc{reinterpret_cast<char*>(mem), 0};
     uint32_t* bits_uT = sc.take<uint32_t>((size_t)r * d_out / 32);
     void* act16 = sc.take<uint16_t>((size_t)T * mx);        // dy.h.gs, then reused
@@ -398,13 +389,104 @@ tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const fl
     // dx' = (b.l.gs) S_V / gs; dx = g.dx'; dg += sum_t x.dx'
     if (e == cudaSuccess) {
         DecSign dec{bits_v, (int64_t)r / 32};
-        EpiArgs ep{dx, nullptr, g, x, colp, (int64_t)d_in, inv_gs};
+        EpiArgs ep{dx, nullptr, g, x, colp, (int64_t)d_in, inv_gs, accumulate};
         e = launch_umma<DecSign, EPI_SCALE_COLSUM>(dec, ep, r16, iT, din, ir, BN, 1, st);
         if (e == cudaSuccess) e = colsum_finish(colp, ttiles, din, dg, st);
     }
     cudaError_t e2 = cudaFreeAsync(mem, st);
-    if (e != cudaSuccess) return cuda_status(e, "blr_backward");
-    return cuda_status(e2, "blr_backward: scratch free");
+    if (e != cudaSuccess) return cuda_status(e, who);
+    return cuda_status(e2, who);
+}
+
+
+bool gscale_ok(float gscale) {
+    int ex = 0;
+    return gscale > 0.f && std::isfinite(gscale) && std::frexp(gscale, &ex) == 0.5f;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq2_status blr_forward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
+                       const float* x, float* y, float* a_save, float* c_save, int64_t T, int64_t d_in, int64_t d_out,
+                       int64_t r, void* stream) {
+    if (!bits_u || !bits_v || !h || !l || !g || !x || !y || !a_save)
+        return blr_fail(TQ2_EINVAL, "blr_forward: null pointer");
+    tq2_status s = check_shapes("blr_forward", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!aligned16(x) || !aligned16(g) || !aligned16(l))
+        return blr_fail(TQ2_EINVAL, "blr_forward: x, g and l must be 16-byte aligned");
+    return forward_one("blr_forward", bits_u, bits_v, h, l, g, x, y, a_save, c_save, T, d_in, d_out, r, 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, const float* h, const float* l, const float* g,
+                        const float* x, const float* dy, const float* a_save, const float* c_save, float* dx, float* dh,
+                        float* dl, float* dg, int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale,
+                        void* stream) {
+    if (!bits_u || !bits_v || !h || !l || !g || !x || !dy || !a_save || !dx || !dh || !dl || !dg)
+        return blr_fail(TQ2_EINVAL, "blr_backward: null pointer");
+    tq2_status s = check_shapes("blr_backward", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!gscale_ok(gscale)) return blr_fail(TQ2_EINVAL, "blr_backward: gscale must be a positive power of two");
+    if (!aligned16(dy) || !aligned16(h) || !aligned16(l) || !aligned16(a_save))
+        return blr_fail(TQ2_EINVAL, "blr_backward: dy, h, l and a_save must be 16-byte aligned");
+    return backward_one("blr_backward", bits_u, bits_v, h, l, g, x, dy, a_save, c_save, dx, dh, dl, dg, T, d_in, d_out,
+                        r, gscale, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tq2_status blr_forward_paths(const blr_path* paths, int P, const float* x, float* y, int64_t T, int64_t d_in,
+                             int64_t d_out, int64_t r, void* stream) {
+    if (!paths || !x || !y) return blr_fail(TQ2_EINVAL, "blr_forward_paths: null pointer");
+    if (P < 1 || P > BLR_MAX_PATHS)
+        return (tq2_status)set_error(TQ2_EINVAL, "blr_forward_paths: need 1 <= P <= 64 (P=%d)", P);
+    tq2_status s = check_shapes("blr_forward_paths", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!aligned16(x)) return blr_fail(TQ2_EINVAL, "blr_forward_paths: x must be 16-byte aligned");
+    for (int p = 0; p < P; ++p) {
+        const blr_path& q = paths[p];
+        if (!q.bits_u || !q.bits_v || !q.h || !q.l || !q.g || !q.a_save)
+            return (tq2_status)set_error(TQ2_EINVAL, "blr_forward_paths: null pointer in path %d", p);
+        if (!aligned16(q.g) || !aligned16(q.l))
+            return (tq2_status)set_error(TQ2_EINVAL, "blr_forward_paths: g and l of path %d must be 16-byte aligned",
+                                         p);
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int p = 0; p < P; ++p) {
+        const blr_path& q = paths[p];
+        s = forward_one("blr_forward_paths", q.bits_u, q.bits_v, q.h, q.l, q.g, x, y, q.a_save, q.c_save, T, d_in,
+                        d_out, r, p > 0 ? 1 : 0, st);
+        if (s != TQ2_OK) return s;
+    }
+    return TQ2_OK;
+}
+
+tq2_status blr_backward_paths(const blr_path* paths, int P, const float* x, const float* dy, float* dx, int64_t T,
+                              int64_t d_in, int64_t d_out, int64_t r, float gscale, void* stream) {
+    if (!paths || !x || !dy || !dx) return blr_fail(TQ2_EINVAL, "blr_backward_paths: null pointer");
+    if (P < 1 || P > BLR_MAX_PATHS)
+        return (tq2_status)set_error(TQ2_EINVAL, "blr_backward_paths: need 1 <= P <= 64 (P=%d)", P);
+    tq2_status s = check_shapes("blr_backward_paths", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!gscale_ok(gscale)) return blr_fail(TQ2_EINVAL, "blr_backward_paths: gscale must be a positive power of two");
+    if (!aligned16(dy)) return blr_fail(TQ2_EINVAL, "blr_backward_paths: dy must be 16-byte aligned");
+    for (int p = 0; p < P; ++p) {
+        const blr_path& q = paths[p];
+        if (!q.bits_u || !q.bits_v || !q.h || !q.l || !q.g || !q.a_save || !q.dh || !q.dl || !q.dg)
+            return (tq2_status)set_error(TQ2_EINVAL, "blr_backward_paths: null pointer in path %d", p);
+        if (!aligned16(q.h) || !aligned16(q.l) || !aligned16(q.a_save))
+            return (tq2_status)set_error(TQ2_EINVAL,
+                                         "blr_backward_paths: h, l and a_save of path %d must be 16-byte aligned", p);
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int p = 0; p < P; ++p) {
+        const blr_path& q = paths[p];
+        s = backward_one("blr_backward_paths", q.bits_u, q.bits_v, q.h, q.l, q.g, x, dy, q.a_save, q.c_save, dx, q.dh,
+                         q.dl, q.dg, T, d_in, d_out, r, gscale, p > 0 ? 1 : 0, st);
+        if (s != TQ2_OK) return s;
+    }
+    return TQ2_OK;
 }
 
 }  // extern "C"

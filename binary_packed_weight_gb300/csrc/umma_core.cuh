@@ -150,7 +150,7 @@ enum EpiMode : int {
     EPI_STORE = 0,        // out[t][n] = acc * oscale
     EPI_ATOMIC = 1,       // out[t][n] += acc * oscale (atomic; two K splits at most)
     EPI_PARTIAL = 2,      // out[z][t][n] = acc (split-K partial, z = blockIdx.z)
-    EPI_SCALE = 3,        // out[t][n] = acc * oscale * vec[n]; out2[t][n] = acc * oscale if out2
+    EPI_SCALE = 3,        // out[t][n] (+)= acc * oscale * vec[n]; out2[t][n] = acc * oscale if out2
     EPI_SCALE_COLSUM = 4, // as EPI_SCALE, plus colpart[tile][n] = sum_t acc*oscale*other[t][n]
     EPI_COLSUM = 5        // colpart[tile][n] = sum_t acc*oscale*other[t][n] only
 };
@@ -163,6 +163,7 @@ struct EpiArgs {
     float* colpart;        // [token tiles][ldo]
     int64_t ldo;           // row stride of out / out2 / other (= plane rows)
     float oscale;
+    int accumulate;        // EPI_SCALE*: out = fl(out + fl(w * vec)) instead of fl(w * vec)
 };
 
 // ----------------------------------------------------------------- kernel ----
@@ -420,7 +421,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                     } else {
                         const float w = a * ep.oscale;
                         if (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) {
-                            ep.out[o] = w * vs;
+                            // product and sum rounded separately (no fused multiply-add):
+                            // the rounding of the pages' multi-path combine
+                            const float pv = __fmul_rn(w, vs);
+                            ep.out[o] = ep.accumulate ? __fadd_rn(ep.out[o], pv) : pv;
                             if (MODE == EPI_SCALE && ep.out2) ep.out2[o] = w;
                         }
                         if (MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) colacc = fmaf(w, ep.other[o], colacc);

@@ -291,6 +291,58 @@ TQ2_API tq2_status blr_backward(const uint32_t* bits_u, const uint32_t* bits_v, 
                         float* dl, float* dg, int64_t T, int64_t d_in, int64_t d_out,
                         int64_t r, float gscale, void* stream);
 
+/*
+ * Several paths of one blr layer, y = sum_p diag(h_p) S_U,p diag(l_p) S_V,p^T
+ * diag(g_p) x.  Passage: blr_forward / blr_backward over layer.paths and the
+ * two-path combine scale_acc2 ("cortiq-engine 0.8.43, train_mm.rs"): the
+ * paths are taken in order, the first writes y (dx) and each later one adds
+ * its product to it, each product and each sum rounded to f32 separately
+ * (no fused multiply-add): for two paths y = fl(fl(h0.c0) + fl(h1.c1)), the
+ * page's one-pass two-path rounding; for more, fl(fl(y + fl(h_p.c_p))) in
+ * path order, as the page's scale_acc passes.
+ *
+ * One path: its bitmaps and vectors (DEVICE, layouts as blr_forward), its
+ * forward outputs a_save (required) and c_save (may be NULL), and its
+ * gradient accumulators dh, dl, dg (DEVICE, += as in blr_backward; used by
+ * blr_backward_paths only).
+ */
+typedef struct {
+    const uint32_t* bits_u;
+    const uint32_t* bits_v;
+    const float* h;
+    const float* l;
+    const float* g;
+    float* a_save;
+    float* c_save;
+    float* dh;
+    float* dl;
+    float* dg;
+} blr_path;
+
+#define BLR_MAX_PATHS 64
+
+/*
+ * blr_forward_paths -- forward of a layer of P paths (1 <= P <= BLR_MAX_PATHS).
+ *   paths   HOST array of P blr_path (read during the call only).
+ *   x       DEVICE float[T][d_in], shared by all paths.
+ *   y       DEVICE float[T][d_out], overwritten with the combined output.
+ * Shape rules as blr_forward.  x and each path's g and l must be 16-byte
+ * aligned.  With P = 1 the result is blr_forward's bit for bit.
+ */
+TQ2_API tq2_status blr_forward_paths(const blr_path* paths, int P, const float* x, float* y, int64_t T,
+                             int64_t d_in, int64_t d_out, int64_t r, void* stream);
+
+/*
+ * blr_backward_paths -- backward of the layer of the last blr_forward_paths
+ * on the same x: each path's dh, dl, dg accumulate (+=), dx (DEVICE
+ * float[T][d_in]) is overwritten with sum_p g_p.dx'_p rounded as described
+ * above.  gscale as blr_backward; dy and each path's h, l and a_save must be
+ * 16-byte aligned.
+ */
+TQ2_API tq2_status blr_backward_paths(const blr_path* paths, int P, const float* x, const float* dy, float* dx,
+                              int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -90,3 +90,32 @@ def abs_chain(h, l, g, x, dy):
     dla = (aa * ba).sum(axis=0)
     dga = (x * dxpa).sum(axis=0)
     return ya, aa, dxa, ba, dha, dla, dga
+
+
+def forward_paths(paths, x):
+    """Several paths of one layer ("cortiq-engine 0.8.43, train_mm.rs",
+    ``blr_forward`` over ``layer.paths``): ``y = sum_p h_p . c_p``.
+
+    ``paths`` is a list of dicts with ``bits_u, bits_v, h, l, g``.  Exact in
+    f64 (the sum's order does not matter here); returns ``(y, [(a_p, c_p)])``.
+    """
+    y = None
+    saved = []
+    for p in paths:
+        yp, a, c = forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x)
+        y = yp if y is None else y + yp
+        saved.append((a, c))
+    return y, saved
+
+
+def backward_paths(paths, x, dy):
+    """Backward of :func:`forward_paths` (``blr_backward`` over the paths):
+    ``dx = sum_p g_p . dx'_p``; each path's ``(dh, dl, dg)`` increments are
+    those of its own single-path backward with the shared ``dy``."""
+    dx = None
+    grads = []
+    for p in paths:
+        dxp, dh, dl, dg, _, _ = backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x, dy)
+        dx = dxp if dx is None else dx + dxp
+        grads.append((dh, dl, dg))
+    return dx, grads

@@ -160,3 +160,69 @@ def test_blr_rejects_bad_arguments(lib):
     # gscale must be a positive power of two
     for gs in (3.0, 0.0, -2.0):
         assert L.blr_backward(pz, pz, pz, pz, pz, pz, pz, pz, None, pz, pz, pz, pz, 4, 64, 64, 128, gs, None) == 1
+
+
+# ---- several paths of one layer (blr_forward_paths / blr_backward_paths)
+
+def _dev_path(p, T, d_out, r, d_in):
+    import torch
+    f = dict(dtype=torch.float32, device="cuda")
+    return dict(bits_u=to_dev(p["bits_u"].view(np.int32)), bits_v=to_dev(p["bits_v"].view(np.int32)),
+                h=to_dev(p["h"]), l=to_dev(p["l"]), g=to_dev(p["g"]),
+                a_save=torch.full((T, r), float("nan"), **f), c_save=torch.full((T, d_out), float("nan"), **f),
+                dh=torch.zeros(d_out, **f), dl=torch.zeros(r, **f), dg=torch.zeros(d_in, **f))
+
+
+def _run_paths(lib, ps, gscale=1.0):
+    import torch
+    T, d_in = ps[0]["x"].shape
+    d_out, r = ps[0]["h"].size, ps[0]["l"].size
+    dps = [_dev_path(p, T, d_out, r, d_in) for p in ps]
+    x, dy = to_dev(ps[0]["x"]), to_dev(ps[0]["dy"])
+    y = torch.full((T, d_out), float("nan"), dtype=torch.float32, device="cuda")
+    dx = torch.full((T, d_in), float("nan"), dtype=torch.float32, device="cuda")
+    lib.blr_forward_paths(dps, x, y)
+    lib.blr_backward_paths(dps, x, dy, dx, gscale=gscale)
+    lib.device_status()
+    n = lambda t: t.cpu().numpy().astype(np.float64)
+    return n(y), n(dx), [(n(d["dh"]), n(d["dl"]), n(d["dg"])) for d in dps], (y, dx)
+
+
+@pytest.mark.parametrize("P", [2, 3])
+def test_paths_against_oracle(lib, P):
+    ps = [_page_inputs(pi=i) for i in range(P)]
+    y, dx, grads, _ = _run_paths(lib, ps, gscale=1024.0)
+    want_y, _ = oblr.forward_paths(ps, ps[0]["x"])
+    want_dx, want_grads = oblr.backward_paths(ps, ps[0]["x"], ps[0]["dy"])
+    chains = [oblr.abs_chain(p["h"], p["l"], p["g"], p["x"], p["dy"]) for p in ps]
+    ya, dxa = sum(c[0] for c in chains), sum(c[2] for c in chains)
+    _check(dict(y=y, dx=dx), dict(y=want_y, dx=want_dx), dict(y=ya, dx=dxa), f"{P} paths")
+    for i, (got, want, c) in enumerate(zip(grads, want_grads, chains)):
+        _check(dict(dh=got[0], dl=got[1], dg=got[2]), dict(dh=want[0], dl=want[1], dg=want[2]),
+               dict(dh=c[4], dl=c[5], dg=c[6]), f"{P} paths, path {i}")
+
+
+def test_paths_combine_rounds_as_the_page(lib):
+    """y = fl(fl(y0 + y1) + y2) and dx likewise, from the single-path results:
+    each product and each sum rounded to f32 separately (the page's scale_acc
+    passes; for two paths its one-pass scale_acc2)."""
+    ps = [_page_inputs(pi=i) for i in range(3)]
+    singles = [_run(lib, p) for p in ps]
+    import torch
+    for P in (2, 3):
+        _, _, _, (y, dx) = _run_paths(lib, ps[:P])
+        want_y, want_dx = np.float32(singles[0]["y"]), np.float32(singles[0]["dx"])
+        for s in singles[1:P]:
+            want_y = (want_y + np.float32(s["y"])).astype(np.float32)
+            want_dx = (want_dx + np.float32(s["dx"])).astype(np.float32)
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), want_y.view(np.uint32)), P
+        assert np.array_equal(dx.cpu().numpy().view(np.uint32), want_dx.view(np.uint32)), P
+
+
+def test_paths_one_path_is_the_single_call(lib):
+    p = _page_inputs()
+    single = _run(lib, p)
+    y, dx, grads, _ = _run_paths(lib, [p])
+    assert np.array_equal(y, single["y"]) and np.array_equal(dx, single["dx"])
+    assert np.array_equal(grads[0][0], single["dh"]) and np.array_equal(grads[0][1], single["dl"])
+    assert np.array_equal(grads[0][2], single["dg"])

@@ -137,3 +137,52 @@ def test_abs_chain_bounds_terms():
     dx, dh, dl, dg, b, _ = blr.backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"], p["dy"])
     for v, bound in ((y, ya), (a, aa), (dx, dxa), (b, ba), (dh, dha), (dl, dla), (dg, dga)):
         assert np.all(np.abs(v) <= bound * (1 + 1e-12))
+
+
+# ---- several paths of one layer (blr_forward / blr_backward over layer.paths)
+
+def _paths(P, key, T=5, d_in=64, d_out=64, r=128):
+    ps = [synth.blr_inputs(T, d_in, d_out, r, key + 10 * i) for i in range(P)]
+    return ps, ps[0]["x"], ps[0]["dy"]
+
+
+def test_paths_single_equals_one_path():
+    ps, x, dy = _paths(1, 700)
+    y, saved = blr.forward_paths(ps, x)
+    y1, a1, c1 = blr.forward(ps[0]["bits_u"], ps[0]["bits_v"], ps[0]["h"], ps[0]["l"], ps[0]["g"], x)
+    assert np.array_equal(y, y1) and np.array_equal(saved[0][0], a1) and np.array_equal(saved[0][1], c1)
+    dx, grads = blr.backward_paths(ps, x, dy)
+    dx1, dh1, dl1, dg1, _, _ = blr.backward(ps[0]["bits_u"], ps[0]["bits_v"], ps[0]["h"], ps[0]["l"], ps[0]["g"], x, dy)
+    assert np.array_equal(dx, dx1)
+    assert all(np.array_equal(u, v) for u, v in zip(grads[0], (dh1, dl1, dg1)))
+
+
+def test_paths_identical_double_and_negated_h_cancels():
+    ps, x, dy = _paths(1, 710)
+    p = ps[0]
+    y2, _ = blr.forward_paths([p, p], x)
+    y1, _, _ = blr.forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x)
+    assert np.array_equal(y2, 2.0 * y1)                       # exact: doubling in f64
+    neg = dict(p, h=-np.asarray(p["h"]))
+    y0, _ = blr.forward_paths([p, neg], x)
+    assert np.array_equal(y0, np.zeros_like(y0))
+    dx0, _ = blr.backward_paths([p, neg], x, dy)             # L = sum y.dy vanishes identically
+    assert np.array_equal(dx0, np.zeros_like(dx0))
+
+
+def test_paths_gradients_are_per_path_and_dx_sums():
+    ps, x, dy = _paths(3, 720)
+    dx, grads = blr.backward_paths(ps, x, dy)
+    total = 0.0
+    for p, (dh, dl, dg) in zip(ps, grads):
+        dxp, dhp, dlp, dgp, _, _ = blr.backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x, dy)
+        assert np.array_equal(dh, dhp) and np.array_equal(dl, dlp) and np.array_equal(dg, dgp)
+        total = total + dxp
+    assert np.allclose(dx, total, rtol=0, atol=1e-12 * np.abs(total).max())
+    # the layer's loss L = sum(y.dy) has dL/dx = dx: check one entry by a central difference
+    x = np.asarray(x, dtype=np.float64)                      # steps exact in f64 (the layer is linear in x)
+    e = np.zeros_like(x); e[2, 7] = 1e-3
+    yp, _ = blr.forward_paths(ps, x + e)
+    ym, _ = blr.forward_paths(ps, x - e)
+    fd = (np.sum(yp * dy) - np.sum(ym * dy)) / 2e-3
+    assert abs(fd - dx[2, 7]) <= 1e-9 * max(1.0, abs(fd))
