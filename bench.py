@@ -273,16 +273,24 @@ def extra_blr(torch, bpw, stream, dev, pk):
     def step():
         fwd()
         bwd()
+    gu, gv = torch.empty((dout, r), **f), torch.empty((din, r), **f)
+
+    def sgn():
+        bpw.blr_sign_grads(bu, d["h"], d["l"], d["g"], d["x"], d["dy"], a, gu, gv, stream=stream.cuda_stream)
     tf, _ = time_graph(torch, fwd, 20, 3, stream)
     tb, _ = time_graph(torch, bwd, 20, 3, stream)
     ts, _ = time_graph(torch, step, 20, 3, stream)
-    tf, tb, ts = tf / 20, tb / 20, ts / 20
+    tg, _ = time_graph(torch, sgn, 20, 3, stream)
+    tf, tb, ts, tg = tf / 20, tb / 20, ts / 20, tg / 20
+    sflops = 3 * 2.0 * T * dout * r                     # b, G_U and G_V: three GEMMs of 2*T*4096*512
     flops = 4 * 2.0 * T * din * r                       # four GEMMs of 2*T*4096*512 (c recomputed: a fifth)
     alg_bytes = 5 * T * din * 4 + 2 * dout * r // 8 + 2 * T * r * 4
     return dict(fwd_us=tf * 1e6, bwd_us=tb * 1e6, step_us=ts * 1e6, tflops=flops / ts / 1e12,
                 alg_gbs=alg_bytes / ts / 1e9, hbm_frac=alg_bytes / ts / 1e9 / pk["hbm"],
                 tensor_frac=flops / ts / 1e12 / pk["bf16"], algorithmic_bytes=alg_bytes, flops=flops,
-                note="forward + backward of one path; dh from a recomputed c (no c_save)")
+                note="forward + backward of one path; dh from a recomputed c (no c_save)",
+                sign_grads_us=tg * 1e6, sign_grads_tflops=sflops / tg / 1e12,
+                sign_grads_tensor_frac=sflops / tg / 1e12 / pk["bf16"])
 
 
 def extra_large(torch, bpw, stream, dev, pk):

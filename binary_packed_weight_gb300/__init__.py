@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
-    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths",
+    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths", "blr_sign_grads",
     "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -45,6 +45,7 @@ _SIGS = {
                           _I64, _I64, _I64, _I64, _F, _P]),
     "blr_forward_paths": (_I, [_P, _I, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "blr_backward_paths": (_I, [_P, _I, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _P]),
+    "blr_sign_grads": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _P]),
 }
 
 
@@ -226,6 +227,15 @@ def blr_backward_paths(paths, x, dy, dx, gscale=1.0, stream=None):
     _check(load().blr_backward_paths(ctypes.cast(arr, _P), len(paths), _ptr(x), _ptr(dy), _ptr(dx), T, d_in, d_out,
                                      r, float(gscale), _stream(stream)), "blr_backward_paths")
     return dx
+
+
+def blr_sign_grads(bits_u, h, l, g, x, dy, a_save, gu, gv, gscale=1.0, stream=None):
+    """G_U [d_out, r] and G_V [d_in, r] of one path (see include/tq2.h)."""
+    T, d_in = x.shape
+    d_out, r = h.numel(), l.numel()
+    _check(load().blr_sign_grads(_ptr(bits_u), _ptr(h), _ptr(l), _ptr(g), _ptr(x), _ptr(dy), _ptr(a_save), _ptr(gu),
+                                 _ptr(gv), T, d_in, d_out, r, float(gscale), _stream(stream)), "blr_sign_grads")
+    return gu, gv
 
 
 def device_status(stream=None):

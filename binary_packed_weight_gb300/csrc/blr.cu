@@ -151,6 +151,27 @@ __global__ void finish_splitk_kernel(const float* __restrict__ part, int S, int 
     }
 }
 
+// dst[c][t] = f16(src[t][c] * col[c] * scale) for t < T and 0 for T <= t < Tp:
+// an operand of a GEMM over the token axis, transposed so that the tokens
+// are its K (natural order, as DecDense and the TMA-loaded side expect).
+// 32 x 32 tiles through shared memory, block (32, 8).
+__global__ void stage_t16_kernel(const float* __restrict__ src, int T, int C, const float* __restrict__ col,
+                                 float scale, uint16_t* __restrict__ dst, int Tp) {
+    __shared__ float tile[32][33];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32, tx = threadIdx.x, ty = threadIdx.y;
+    for (int i = ty; i < 32; i += 8) {
+        const int t = t0 + i, c = c0 + tx;
+        tile[i][tx] = (t < T && c < C) ? src[(int64_t)t * C + c] * col[c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, t = t0 + tx;
+        if (c < C && t < Tp) dst[(int64_t)c * Tp + t] = __half_as_ushort(__float2half_rn(tile[tx][i] * scale));
+    }
+}
+
 // colpart[chunk][n] = sum over the chunk's tokens of A[t][n] * B[t][n]
 // (block (32, 8) as finish_splitk_kernel; fixed order).
 __global__ void colsum_prod_kernel(const float* __restrict__ A, const float* __restrict__ B, int T, int n,
@@ -487,6 +508,82 @@ tq2_status blr_backward_paths(const blr_path* paths, int P, const float* x, cons
         if (s != TQ2_OK) return s;
     }
     return TQ2_OK;
+}
+
+tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l, const float* g, const float* x,
+                          const float* dy, const float* a_save, float* gu, float* gv, int64_t T, int64_t d_in,
+                          int64_t d_out, int64_t r, float gscale, void* stream) {
+    if (!bits_u || !h || !l || !g || !x || !dy || !a_save || !gu || !gv)
+        return blr_fail(TQ2_EINVAL, "blr_sign_grads: null pointer");
+    tq2_status s = check_shapes("blr_sign_grads", T, d_in, d_out, r);
+    if (s != TQ2_OK) return s;
+    if (!gscale_ok(gscale)) return blr_fail(TQ2_EINVAL, "blr_sign_grads: gscale must be a positive power of two");
+    if (!aligned16(dy) || !aligned16(h))
+        return blr_fail(TQ2_EINVAL, "blr_sign_grads: dy and h must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
+    const int Tp = (iT + 63) / 64 * 64, BN = umma_pick_bn(iT), chunks = (iT + FIN_TC - 1) / FIN_TC;
+    const int S = pick_splits(ir, iT, dout, BN);
+    const int64_t mx = d_in > d_out ? d_in : d_out;
+    const size_t bytes = (size_t)r * d_out / 8 + 256 + (size_t)T * d_out * 2 + 256 + (size_t)S * T * r * 4 + 256 +
+                         (size_t)T * r * 4 + 256 + (size_t)T * r * 2 + 256 + (size_t)(mx + r) * Tp * 2 + 512;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocAsync(&mem, bytes, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_sign_grads: scratch");
+    Scratch sc{reinterpret_cast<char*>(mem), 0};
+    uint32_t* bits_uT = sc.take<uint32_t>((size_t)r * d_out / 32);
+    void* act16 = sc.take<uint16_t>((size_t)T * d_out);
+    float* part = sc.take<float>((size_t)S * T * r);
+    float* b32 = sc.take<float>((size_t)T * r);
+    uint16_t* b16 = sc.take<uint16_t>((size_t)T * r);      // the finish kernel's f16 staging (unused here)
+    uint16_t* big = sc.take<uint16_t>((size_t)mx * Tp);     // (dy.h.gs)^T, then (x.g)^T
+    uint16_t* small = sc.take<uint16_t>((size_t)r * Tp);    // (a.l)^T, then (b.l.gs)^T
+    const float inv_gs = 1.0f / gscale;
+    auto stage_t = [&](const float* src, int C, const float* col, float scale, uint16_t* dst) {
+        return launch_pdl(stage_t16_kernel, dim3((unsigned)((C + 31) / 32), (unsigned)(Tp / 32)), dim3(32, 8), 0, st,
+                          src, iT, C, col, scale, dst, Tp);
+    };
+    // G[o][k] = (1/gs) sum_t rowsT[o][t] colsT[k][t]: A = colsT (r rows, DecDense), B = rowsT
+    // (o tokens, TMA); the core writes out[token][row] = G[o][k].  Two K splits (atomic
+    // add into a zeroed G, order-independent for two) when one split leaves SMs idle.
+    auto gemm = [&](const uint16_t* colsT, const uint16_t* rowsT, int nrows, float* G) -> cudaError_t {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int bn = umma_pick_bn(nrows);
+        const int tiles = ((ir + UM_BM - 1) / UM_BM) * ((nrows + bn - 1) / bn);
+        DecDense dec{colsT, (int64_t)Tp};
+        EpiArgs ep{G, nullptr, nullptr, nullptr, nullptr, (int64_t)r, inv_gs};
+        if (tiles < sms && Tp >= 2 * UM_BK) {
+            cudaError_t e1 = cudaMemsetAsync(G, 0, (size_t)nrows * r * sizeof(float), st);
+            if (e1 != cudaSuccess) return e1;
+            return launch_umma<DecDense, EPI_ATOMIC>(dec, ep, rowsT, nrows, ir, Tp, bn, 2, st);
+        }
+        return launch_umma<DecDense, EPI_STORE>(dec, ep, rowsT, nrows, ir, Tp, bn, 1, st);
+    };
+    // b = (dy.h.gs) S_U / gs, as in the backward
+    e = transpose_bits(bits_u, bits_uT, dout, ir, st);
+    if (e == cudaSuccess) e = stage32(dy, h, gscale, act16, iT, dout, st);
+    if (e == cudaSuccess) {
+        DecSign dec{bits_uT, (int64_t)d_out / 32};
+        EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
+        e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, act16, iT, ir, dout, BN, S, st);
+    }
+    if (e == cudaSuccess)
+        e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
+                       (const float*)part, S, iT, ir, inv_gs, b32, l, gscale, b16, (const float*)nullptr,
+                       (float*)nullptr);
+    // G_U = diag(h) dy^T a diag(l), from (dy.h.gs)^T and (a.l)^T
+    if (e == cudaSuccess) e = stage_t(dy, dout, h, gscale, big);
+    if (e == cudaSuccess) e = stage_t(a_save, ir, l, 1.0f, small);
+    if (e == cudaSuccess) e = gemm(small, big, dout, gu);
+    // G_V = diag(g) x^T b diag(l), from (x.g)^T and (b.l.gs)^T
+    if (e == cudaSuccess) e = stage_t(x, din, g, 1.0f, big);
+    if (e == cudaSuccess) e = stage_t(b32, ir, l, gscale, small);
+    if (e == cudaSuccess) e = gemm(small, big, din, gv);
+    cudaError_t e2 = cudaFreeAsync(mem, st);
+    if (e != cudaSuccess) return cuda_status(e, "blr_sign_grads");
+    return cuda_status(e2, "blr_sign_grads: scratch free");
 }
 
 }  // extern "C"

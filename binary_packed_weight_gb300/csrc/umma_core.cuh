@@ -88,6 +88,8 @@ struct DecTQ2 {
     const uint16_t* scales;    // [rows][K/128]
     int64_t pitch;             // K/4
     int nb;                    // K/128
+    static constexpr int PF = 3;   // stages each decoder warp loads ahead
+    static constexpr bool PRIOR = false;   // rows written by earlier work on the stream (wait for it)
     struct Raw { uint4 c; uint16_t d; };
     __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
         Raw r;
@@ -122,6 +124,8 @@ struct DecTQ2 {
 struct DecSign {
     const uint32_t* bits;      // [rows][K/32]
     int64_t words;             // K/32
+    static constexpr int PF = 3;
+    static constexpr bool PRIOR = false;
     struct Raw { uint2 w; };
     __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
         Raw r;
@@ -142,6 +146,33 @@ struct DecSign {
     __device__ __forceinline__ void decode(const Raw& r, uint32_t (&v)[32]) const {
         word(r.w.x, v);
         word(r.w.y, v + 16);
+    }
+};
+
+// Dense f16 rows, already in the K order the activations are staged in
+// (pair j of a stage = elements 2j, 2j+1): the decoder only moves them.  A
+// stage is 128 bytes per row, so one stage is loaded ahead.
+struct DecDense {
+    const uint16_t* rows;      // [rows][pitch] f16 bits
+    int64_t pitch;             // elements per row (a multiple of 64)
+    static constexpr int PF = 1;
+    static constexpr bool PRIOR = true;    // staged by the kernel before this one
+    struct Raw { uint4 q[8]; };
+    __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
+        Raw r;
+        const uint4* src = reinterpret_cast<const uint4*>(rows + (int64_t)row * pitch + (int64_t)kc * 64);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = ok ? ldg_u4_l1(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        return r;
+    }
+    __device__ __forceinline__ void decode(const Raw& r, uint32_t (&v)[32]) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[4 * i] = r.q[i].x;
+            v[4 * i + 1] = r.q[i].y;
+            v[4 * i + 2] = r.q[i].z;
+            v[4 * i + 3] = r.q[i].w;
+        }
     }
 };
 
@@ -301,7 +332,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
         // warp pair (q, h): lane quarter q, stages with item parity h
         const int q = warp & 3, h = (warp - 4) >> 2;
         const int arow = q * 32 + lane;                    // row of the A stage this thread writes
-        constexpr int PF = 3;                              // own items prefetched ahead
+        constexpr int PF = Dec::PF;                        // own items prefetched ahead
         // flattened walk over this CTA's (tile, kc) items, two cursors
         struct Cur {
             int t, kc, k1, row;
@@ -322,6 +353,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             if (++c.kc >= c.k1) start(c, c.t + units);
         };
         Cur ld, pr;
+        if (Dec::PRIOR) pdl_wait();                        // the rows come from the previous kernel
         start(ld, unit0);
         start(pr, unit0);
         int ld_it = 0;

@@ -343,6 +343,31 @@ TQ2_API tq2_status blr_backward_paths(const blr_path* paths, int P, const float*
                               int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale,
                               void* stream);
 
+/*
+ * blr_sign_grads -- the gradients of the loss with respect to one path's
+ * signs, G_U = diag(h) dy^T a diag(l) ([d_out][r]) and
+ * G_V = diag(g) x^T b diag(l) ([d_in][r]) with b = (dy.h) S_U.
+ * Passage: blr_backward's sign-training step and the test
+ * blr_sign_flip_exact ("cortiq-engine 0.8.43, train_mm.rs"): the token axis
+ * is the GEMMs' K, the operands dy.h.gs, a.l, x.g and b.l.gs are staged
+ * transposed in f16, and flipping sign s of U[i,k] changes L = 1/2|y - y*|^2
+ * by -2 s G_U[i,k] + 2 h_i^2 l_k^2 sum_t a_tk^2 (V likewise).
+ *
+ *   bits_u        DEVICE uint32[d_out][r/32] (S_U; S_V is not needed)
+ *   h, l, g       DEVICE float[d_out], float[r], float[d_in]
+ *   x, dy         DEVICE float[T][d_in], float[T][d_out]
+ *   a_save        DEVICE float[T][r] from blr_forward on the same x
+ *   gu, gv        DEVICE float[d_out][r], float[d_in][r], overwritten
+ *   gscale        power of two multiplying the dy-side operands while they
+ *                 are staged in f16, divided back out (as blr_backward);
+ *                 dy.h.gs and b.l.gs must stay inside the f16 range (a
+ *                 value beyond 65504 stages as inf).
+ * Shape rules as blr_forward; dy and h must be 16-byte aligned.
+ */
+TQ2_API tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l, const float* g,
+                          const float* x, const float* dy, const float* a_save, float* gu, float* gv,
+                          int64_t T, int64_t d_in, int64_t d_out, int64_t r, float gscale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -119,3 +119,22 @@ def backward_paths(paths, x, dy):
         dx = dxp if dx is None else dx + dxp
         grads.append((dh, dl, dg))
     return dx, grads
+
+
+def sign_grads(bits_u, bits_v, h, l, g, x, dy):
+    """Gradients of ``L`` with respect to one path's signs ("cortiq-engine
+    0.8.43, train_mm.rs", ``blr_backward`` with sign training):
+    ``G_U = diag(h) dy^T a diag(l)`` and ``G_V = diag(g) x^T b diag(l)`` with
+    ``a = (x.g) S_V`` and ``b = (dy.h) S_U``.  Returns ``(G_U, G_V)``,
+    ``[d_out][r]`` and ``[d_in][r]``."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    h = np.asarray(h, dtype=np.float64)
+    l = np.asarray(l, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    _, a, _ = forward(bits_u, bits_v, h, l, g, x)
+    S_U = expand_bits(bits_u, h.size, l.size)
+    b = (dy * h[None, :]) @ S_U
+    G_U = h[:, None] * (dy.T @ a) * l[None, :]
+    G_V = g[:, None] * (x.T @ b) * l[None, :]
+    return G_U, G_V

@@ -226,3 +226,40 @@ def test_paths_one_path_is_the_single_call(lib):
     assert np.array_equal(y, single["y"]) and np.array_equal(dx, single["dx"])
     assert np.array_equal(grads[0][0], single["dh"]) and np.array_equal(grads[0][1], single["dl"])
     assert np.array_equal(grads[0][2], single["dg"])
+
+
+# ---- sign gradients (blr_sign_grads) against the oracle
+
+SIGN_TOL = 2.0 ** -8      # a (or b) and two staged operands: three f16 roundings per product chain
+
+
+@pytest.mark.parametrize("shape", [(70, 384, 256, 128), (33, 192, 320, 256), (2048, 4096, 4096, 512)],
+                         ids=["page", "ragged", "C5"])
+def test_sign_grads_against_oracle(lib, shape):
+    import torch
+    T, d_in, d_out, r = shape
+    p = _page_inputs(T, d_in, d_out, r) if T == 70 else synth.blr_inputs(T, d_in, d_out, r, 900 + T)
+    d = {k: to_dev(v) for k, v in p.items() if k not in ("bits_u", "bits_v")}
+    bu, bv = to_dev(p["bits_u"].view(np.int32)), to_dev(p["bits_v"].view(np.int32))
+    f = dict(dtype=torch.float32, device="cuda")
+    y, a = torch.empty((T, d_out), **f), torch.empty((T, r), **f)
+    lib.blr_forward(bu, bv, d["h"], d["l"], d["g"], d["x"], y, a)
+    gu = torch.full((d_out, r), float("nan"), **f)
+    gv = torch.full((d_in, r), float("nan"), **f)
+    # the page's gradient scale with its 1e-3-sized dy; 1 for unit-sized dy, where
+    # b.l.gs would leave the f16 range at 1024
+    gs = 1024.0 if T == 70 else 1.0
+    lib.blr_sign_grads(bu, d["h"], d["l"], d["g"], d["x"], d["dy"], a, gu, gv, gscale=gs)
+    lib.device_status()
+    GU, GV = oblr.sign_grads(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"], p["dy"])
+    _, aa, _, ba, _, _, _ = oblr.abs_chain(p["h"], p["l"], p["g"], p["x"], p["dy"])
+    h, l, g = (np.abs(np.asarray(p[k], dtype=np.float64)) for k in ("h", "l", "g"))
+    cu = h[:, None] * (np.abs(np.asarray(p["dy"], dtype=np.float64)).T @ aa) * l[None, :]
+    cv = g[:, None] * (np.abs(np.asarray(p["x"], dtype=np.float64)).T @ ba) * l[None, :]
+    for name, got, want, chain in (("G_U", gu, GU, cu), ("G_V", gv, GV, cv)):
+        got = got.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), name
+        rel = np.sqrt(np.sum((got - want) ** 2) / max(np.sum(want * want), 1e-300))
+        assert rel < 3e-3, f"{shape} {name}: relative L2 error {rel:.3e}"
+        bad = np.abs(got - want) > SIGN_TOL * chain + 1e-30
+        assert not bad.any(), f"{shape} {name}: {bad.sum()} elements above 2^-8 of the abs chain"

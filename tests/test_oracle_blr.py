@@ -186,3 +186,39 @@ def test_paths_gradients_are_per_path_and_dx_sums():
     ym, _ = blr.forward_paths(ps, x - e)
     fd = (np.sum(yp * dy) - np.sum(ym * dy)) / 2e-3
     assert abs(fd - dx[2, 7]) <= 1e-9 * max(1.0, abs(fd))
+
+
+# ---- sign gradients, pinned by the page's flip identity (test blr_sign_flip_exact)
+
+def test_sign_gradients_flip_identity():
+    """L = 1/2 |y - y*|^2 is quadratic in each sign, so flipping sign s of
+    U[i,k] changes it by exactly -2 s G_U[i,k] + 2 h_i^2 l_k^2 sum_t a_tk^2,
+    and of V[j,k] by -2 s G_V[j,k] + 2 g_j^2 l_k^2 (sum_t x_tj^2)(sum_i h_i^2).
+    Each flip reruns the forward with the bit changed (this also checks the
+    bit mapping)."""
+    p = synth.blr_inputs(9, 64, 128, 128, 801)
+    x = np.asarray(p["x"], dtype=np.float64)
+    y0, a, _ = blr.forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x)
+    ystar = y0 + 0.7 * np.asarray(synth.normal(y0.size, 802), dtype=np.float64).reshape(y0.shape)
+    dy = y0 - ystar
+    L0 = 0.5 * np.sum((y0 - ystar) ** 2)
+    GU, GV = blr.sign_grads(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], x, dy)
+    h, l, g = (np.asarray(p[k], dtype=np.float64) for k in ("h", "l", "g"))
+    SU = blr.expand_bits(p["bits_u"], h.size, l.size)
+    SV = blr.expand_bits(p["bits_v"], g.size, l.size)
+    for (i, k) in ((0, 0), (1, 31), (2, 32), (127, 127), (17, 63), (100, 64)):
+        for side in ("U", "V"):
+            bits = np.array(p["bits_u" if side == "U" else "bits_v"], dtype=np.uint32).copy()
+            row = i % (h.size if side == "U" else g.size)
+            bits[row, k // 32] ^= np.uint32(1 << (k % 32))
+            bu, bv = (bits, p["bits_v"]) if side == "U" else (p["bits_u"], bits)
+            y1, _, _ = blr.forward(bu, bv, h, l, g, x)
+            dL = 0.5 * np.sum((y1 - ystar) ** 2) - L0
+            if side == "U":
+                s, G = SU[row, k], GU[row, k]
+                quad = 2 * h[row] ** 2 * l[k] ** 2 * np.sum(a[:, k] ** 2)
+            else:
+                s, G = SV[row, k], GV[row, k]
+                quad = 2 * g[row] ** 2 * l[k] ** 2 * np.sum(x[:, row] ** 2) * np.sum(h ** 2)
+            pred = -2 * s * G + quad
+            assert abs(dL - pred) <= 1e-9 * (2 * abs(G) + quad), (side, row, k, dL, pred)
