@@ -7,17 +7,12 @@
 // expanded on chip to (c-1)*d in f16, which is exact (the v10 parity test on
 // that page relies on the same fact), so the block scale needs no epilogue.
 //
-// One CTA computes a 128 (weight rows) x BN (tokens) tile of out^T:
-//   * the MMA's A operand is the decoded weight tile, written straight into
-//     tensor memory by four decoder warps (one weight row per thread, so a
-//     thread's row is its TMEM lane) -- no shared-memory traffic for A;
-//   * the B operand is the f16 activation tile, loaded by TMA with 128-byte
-//     swizzling into a 4-stage shared-memory ring;
-//   * one elected thread issues tcgen05.mma (kind::f16, f32 accumulate) into
-//     a TMEM accumulator of BN columns and commits each stage back to the
-//     producers through mbarriers;
-//   * the decoder warps then read the accumulator with tcgen05.ld and store
-//     out[m][n] (a warp writes 32 consecutive n of one token: 128 bytes).
+// The GEMM runs on the persistent tcgen05 core (umma_core.cuh) with the TQ2
+// decoder: a CTA computes 128 weight rows x BN tokens of out^T; decoder warps
+// write the f16 weight rows into a shared-memory ring in the MMA's swizzled
+// layout, TMA brings the f16 activation tiles, one thread issues the MMAs
+// into two tensor-memory accumulators, and four epilogue warps store
+// out[m][n] while the next tile's MMAs run.
 // The K order inside every 16-element group is permuted the same way on both
 // operands: position 2q holds element q and 2q+1 holds element q+8, which is
 // the order in which two-code pairs fall out of a 32-bit code word.
