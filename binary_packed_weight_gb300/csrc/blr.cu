@@ -154,21 +154,41 @@ __global__ void finish_splitk_kernel(const float* __restrict__ part, int S, int 
 // dst[c][t] = f16(src[t][c] * col[c] * scale) for t < T and 0 for T <= t < Tp:
 // an operand of a GEMM over the token axis, transposed so that the tokens
 // are its K (natural order, as DecDense and the TMA-loaded side expect).
-// 32 x 32 tiles through shared memory, block (32, 8).
-__global__ void stage_t16_kernel(const float* __restrict__ src, int T, int C, const float* __restrict__ col,
-                                 float scale, uint16_t* __restrict__ dst, int Tp) {
-    __shared__ float tile[32][33];
+// 64 x 64 tiles through shared memory, 256 threads: 16-byte loads along c
+// (16 threads a token row), 4-byte stores of two tokens along t (32 threads,
+// 128 bytes, a c row).  C is a multiple of 64 (d_in, d_out, r).
+__global__ void __launch_bounds__(256) stage_t16_kernel(const float* __restrict__ src, int T, int C,
+                                                        const float* __restrict__ col, float scale,
+                                                        uint16_t* __restrict__ dst, int Tp) {
+    __shared__ float tile[64][65];
     pdl_wait();
     pdl_launch_dependents();
-    const int c0 = blockIdx.x * 32, t0 = blockIdx.y * 32, tx = threadIdx.x, ty = threadIdx.y;
-    for (int i = ty; i < 32; i += 8) {
-        const int t = t0 + i, c = c0 + tx;
-        tile[i][tx] = (t < T && c < C) ? src[(int64_t)t * C + c] * col[c] : 0.f;
+    const int c0 = blockIdx.x * 64, t0 = blockIdx.y * 64, tid = threadIdx.x;
+    {
+        const int cq = (tid & 15) * 4, tr = tid >> 4;                  // 4 columns, token row 0..15
+        const float4 cv = *reinterpret_cast<const float4*>(col + c0 + cq);
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int i = tr + 16 * pass, t = t0 + i;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T) v = *reinterpret_cast<const float4*>(src + (int64_t)t * C + c0 + cq);
+            tile[i][cq] = v.x * cv.x;
+            tile[i][cq + 1] = v.y * cv.y;
+            tile[i][cq + 2] = v.z * cv.z;
+            tile[i][cq + 3] = v.w * cv.w;
+        }
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int c = c0 + i, t = t0 + tx;
-        if (c < C && t < Tp) dst[(int64_t)c * Tp + t] = __half_as_ushort(__float2half_rn(tile[tx][i] * scale));
+    {
+        const int tp = (tid & 31) * 2, cr = tid >> 5;                  // two tokens, c row 0..7
+#pragma unroll
+        for (int pass = 0; pass < 8; ++pass) {
+            const int j = cr + 8 * pass, c = c0 + j, t = t0 + tp;
+            if (t < Tp) {
+                const __half2 h2 = __floats2half2_rn(tile[tp][j] * scale, tile[tp + 1][j] * scale);
+                *reinterpret_cast<__half2*>(dst + (int64_t)c * Tp + t) = h2;
+            }
+        }
     }
 }
 
@@ -518,8 +538,8 @@ tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l
     tq2_status s = check_shapes("blr_sign_grads", T, d_in, d_out, r);
     if (s != TQ2_OK) return s;
     if (!gscale_ok(gscale)) return blr_fail(TQ2_EINVAL, "blr_sign_grads: gscale must be a positive power of two");
-    if (!aligned16(dy) || !aligned16(h))
-        return blr_fail(TQ2_EINVAL, "blr_sign_grads: dy and h must be 16-byte aligned");
+    if (!aligned16(dy) || !aligned16(h) || !aligned16(l) || !aligned16(g) || !aligned16(x) || !aligned16(a_save))
+        return blr_fail(TQ2_EINVAL, "blr_sign_grads: x, dy, a_save, h, l and g must be 16-byte aligned");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
     const int Tp = (iT + 63) / 64 * 64, BN = umma_pick_bn(iT), chunks = (iT + FIN_TC - 1) / FIN_TC;
@@ -540,8 +560,8 @@ tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l
     uint16_t* small = sc.take<uint16_t>((size_t)r * Tp);    // (a.l)^T, then (b.l.gs)^T
     const float inv_gs = 1.0f / gscale;
     auto stage_t = [&](const float* src, int C, const float* col, float scale, uint16_t* dst) {
-        return launch_pdl(stage_t16_kernel, dim3((unsigned)((C + 31) / 32), (unsigned)(Tp / 32)), dim3(32, 8), 0, st,
-                          src, iT, C, col, scale, dst, Tp);
+        return launch_pdl(stage_t16_kernel, dim3((unsigned)(C / 64), (unsigned)(Tp / 64)), dim3(256), 0, st, src, iT,
+                          C, col, scale, dst, Tp);
     };
     // G[o][k] = (1/gs) sum_t rowsT[o][t] colsT[k][t]: A = colsT (r rows, DecDense), B = rowsT
     // (o tokens, TMA); the core writes out[token][row] = G[o][k].  Two K splits (atomic

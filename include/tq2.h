@@ -362,7 +362,8 @@ TQ2_API tq2_status blr_backward_paths(const blr_path* paths, int P, const float*
  *                 are staged in f16, divided back out (as blr_backward);
  *                 dy.h.gs and b.l.gs must stay inside the f16 range (a
  *                 value beyond 65504 stages as inf).
- * Shape rules as blr_forward; dy and h must be 16-byte aligned.
+ * Shape rules as blr_forward; x, dy, a_save, h, l and g must be 16-byte
+ * aligned (TQ2_EINVAL otherwise).
  */
 TQ2_API tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l, const float* g,
                           const float* x, const float* dy, const float* a_save, float* gu, float* gv,
