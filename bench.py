@@ -144,6 +144,22 @@ def gemv_bytes(N, K):
     return N * K // 4 + N * (K // 128) * 2
 
 
+def max_over_ranks(torch, dist, secs, device):
+    """The job ends when its slowest rank does: every rank gets the maximum of
+    the ranks' timed-region seconds (unchanged without a process group)."""
+    if dist is None:
+        return secs
+    t = torch.tensor([secs], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_gemv, gemvs_per_rank, world, secs):
+    """Whole-job packed-weight GB/s: the GEMVs of every rank over the slowest
+    rank's seconds (each replica runs the same work: weak scaling)."""
+    return bytes_per_gemv * gemvs_per_rank * world / secs / 1e9
+
+
 # ------------------------------------------------------------- workloads ----
 def capture(torch, fn, stream, warmup):
     with torch.cuda.stream(stream):
@@ -426,15 +442,13 @@ def main():
     e1.synchronize()
     clk = clocks.stop()
     secs = e0.elapsed_time(e1) / 1e3
+    secs = max_over_ranks(torch, dist, secs, dev)
     if dist:
-        t = torch.tensor([secs], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
         dist.barrier()
     N, K, M = ctx["N"], ctx["K"], ctx["M"]
     gemvs = args.steps * GEMV_COPIES
     wbytes = gemv_bytes(N, K)
-    value = wbytes * gemvs * world / secs / 1e9
+    value = job_gbs(wbytes, gemvs, world, secs)
     t_launch = secs / args.steps                      # one grouped launch per step
     alg = GEMV_COPIES * (wbytes + M * K * 4 + M * N * 4)
     achieved = alg / t_launch / 1e9
