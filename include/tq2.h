@@ -124,7 +124,8 @@ TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
  *
  *   x       DEVICE float[M][K], row-major, 16-byte aligned.
  *   out     DEVICE float[M][N], row-major, overwritten.
- *   M       >= 1 (M == 0 is a no-op returning TQ2_OK).
+ *   M       0 <= M <= 2^24 (M == 0 is a no-op returning TQ2_OK); on the
+ *           tensor path also M*K < 2^31.  Else TQ2_ESHAPE.
  *   N, K    must equal the handle's shape, else TQ2_ESHAPE.
  *   stream  asynchronous on this stream.  Internal scratch (f16 copies of
  *           x) is taken from the stream-ordered allocator of the current
@@ -132,7 +133,8 @@ TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
  *
  * M <= 16 runs the skinny kernel: f32 activations split exactly into two
  * f16 terms, f32 accumulation; |error| <= 1e-3 at K <= 4096 for unit-scale
- * data.  For M <= 2 and M*K <= 32768 it is a single kernel with no scratch.  M > 16 runs the tensor-core kernel: activations rounded to f16
+ * data.  For M <= 2 and M*K <= 32768 it is a single kernel with no scratch.
+ * M > 16 runs the tensor-core kernel: activations rounded to f16
  * (nearest-even), weights exact in f16, f32 accumulation;
  * |error| <= 1e-2 * sum_k |x[m,k] W[n,k]|.
  */
@@ -255,8 +257,9 @@ TQ2_API tq2_status blr_expand_bits(const uint32_t* bits, int64_t rows, int64_t r
  *   c_save  DEVICE float[T][d_out] overwritten with c, or NULL (then
  *           blr_backward recomputes c from a_save)
  *   T >= 1; d_in, d_out multiples of 64; r >= 128, r % 128 == 0 (the page
- *   requires a multiple of 128).  Else TQ2_ESHAPE.  x, g and l must be
- *   16-byte aligned (TQ2_EINVAL otherwise).
+ *   requires a multiple of 128); T*max(d_in, d_out) < 2^31, T*r < 2^28 and
+ *   d_in, d_out <= 2^20.  Else TQ2_ESHAPE.  x, g and l must be 16-byte
+ *   aligned (TQ2_EINVAL otherwise).
  * The activations x.g and a.l are staged to f16 (nearest-even); the GEMMs
  * accumulate in f32.  Scratch comes from the stream-ordered allocator.
  */

@@ -34,6 +34,9 @@ def _err(lib):
 def test_tq2_calls(lib):
     assert lib.tq2_gemm(A, A, A, 0, 16, 128, None) == TQ2_OK            # M = 0: nothing to do
     assert lib.tq2_gemm(None, A, A, 1, 16, 128, None) == TQ2_EINVAL
+    assert lib.tq2_gemm(A, None, A, 1, 16, 128, None) == TQ2_EINVAL
+    for M in (-1, (1 << 24) + 1):                                      # refused before the handle is read
+        assert lib.tq2_gemm(A, A, A, M, 16, 128, None) == TQ2_ESHAPE, M
     assert lib.tq2_gemm_path(None, A, A, 1, 16, 128, 1, None) == TQ2_EINVAL
     assert lib.tq2_gemm_skinny_static(None, A, A, 1, 16, 128, None) == TQ2_EINVAL
     assert lib.tq2_shape(None, None, None) == TQ2_EINVAL
