@@ -15,7 +15,7 @@ import os
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
     "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths", "blr_sign_grads",
-    "device_status", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
+    "device_status", "debug_wait_timeout", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
 PATH_AUTO, PATH_SKINNY, PATH_TENSOR = 0, 1, 2
@@ -29,6 +29,7 @@ _SIGS = {
     "tq2_last_error": (ctypes.c_char_p, []),
     "tq2_version": (ctypes.c_char_p, []),
     "tq2_device_status": (_I, [_P]),
+    "tq2_debug_wait_timeout": (_I, [ctypes.c_uint64, _P]),
     "tq2_upload": (_I, [_P, _I64, _I64, ctypes.POINTER(_P), _P]),
     "tq2_free": (_I, [_P]),
     "tq2_shape": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
@@ -236,6 +237,12 @@ def blr_sign_grads(bits_u, h, l, g, x, dy, a_save, gu, gv, gscale=1.0, stream=No
     _check(load().blr_sign_grads(_ptr(bits_u), _ptr(h), _ptr(l), _ptr(g), _ptr(x), _ptr(dy), _ptr(a_save), _ptr(gu),
                                  _ptr(gv), T, d_in, d_out, r, float(gscale), _stream(stream)), "blr_sign_grads")
     return gu, gv
+
+
+def debug_wait_timeout(limit_ns, stream=None):
+    """Launch the test kernel whose bounded wait runs out after ``limit_ns``
+    (see include/tq2.h); the next :func:`device_status` raises TQ2_ETIMEOUT."""
+    _check(load().tq2_debug_wait_timeout(int(limit_ns), _stream(stream)), "tq2_debug_wait_timeout")
 
 
 def device_status(stream=None):

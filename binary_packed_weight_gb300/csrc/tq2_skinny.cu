@@ -368,3 +368,45 @@ extern "C" TQ2_API tq2_status tq2_gemm_skinny_static(tq2_handle h, const float* 
         return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: launch: %s", cudaGetErrorString(e));
     return TQ2_OK;
 }
+
+// --------------------------------------------------------------------------
+// Test export: a bounded device-side wait that runs out.
+//
+// Every wait inside the library's kernels gives up after a bounded time,
+// records the timeout in the device error word and returns, so that a lost
+// hand-off ends as a status (tq2_device_status -> TQ2_ETIMEOUT) instead of a
+// hung GPU.  This kernel exercises that path on purpose and nothing else:
+// one thread initialises a shared-memory mbarrier that expects one arrival,
+// never arrives on it, waits for its first phase with a bound of limit_ns,
+// records the timeout and returns.  It touches no other memory.
+// --------------------------------------------------------------------------
+namespace tq2 {
+namespace {
+
+__global__ void wait_runs_out_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_sleep(&bar, 0u, 1000u)) {       // phase 0 never completes
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout();
+            return;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace tq2
+
+extern "C" TQ2_API tq2_status tq2_debug_wait_timeout(uint64_t limit_ns, void* stream) {
+    if (limit_ns == 0 || limit_ns > tq2::WAIT_LIMIT_NS)
+        return (tq2_status)tq2::set_error(TQ2_EINVAL, "tq2_debug_wait_timeout: need 0 < limit_ns <= %llu",
+                                          (unsigned long long)tq2::WAIT_LIMIT_NS);
+    tq2::wait_runs_out_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_debug_wait_timeout: launch: %s", cudaGetErrorString(e));
+    return TQ2_OK;
+}

@@ -82,6 +82,18 @@ TQ2_API const char* tq2_version(void);
  */
 TQ2_API tq2_status tq2_device_status(void* stream);
 
+/*
+ * tq2_debug_wait_timeout -- test export for the error path above: launches
+ * one thread that waits, with a bound of limit_ns, on a shared-memory
+ * barrier that nothing completes.  When the bound runs out it records the
+ * timeout exactly as the library's kernels do and returns, so the next
+ * tq2_device_status on that stream reports TQ2_ETIMEOUT (and clears it)
+ * while the context stays usable.  Nothing faults, traps or hangs.
+ *   limit_ns  0 < limit_ns <= 1e9 (the kernels' own bound), else TQ2_EINVAL.
+ *   stream    asynchronous on it.
+ */
+TQ2_API tq2_status tq2_debug_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Ternary TQ2 weights                                                       */
 /* ------------------------------------------------------------------------ */

@@ -51,6 +51,11 @@ def test_tq2_calls(lib):
     assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 2, 32768, None) == TQ2_ESHAPE  # M*K <= 32768
 
 
+def test_debug_wait_timeout_bound(lib):
+    assert lib.tq2_debug_wait_timeout(0, None) == TQ2_EINVAL
+    assert lib.tq2_debug_wait_timeout(1_000_000_001, None) == TQ2_EINVAL
+
+
 def test_quantize(lib):
     assert lib.tq2_quantize(None, 1, 128, A, None) == TQ2_EINVAL
     assert lib.tq2_quantize(A, 1, 128, None, None) == TQ2_EINVAL
