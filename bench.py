@@ -391,6 +391,51 @@ def oracle_gemv_sample(budget_s=12.0):
                                       f"in {dt:.1f} s; cpu/wall {cpu / dt:.2f}")
 
 
+def oracle_samples(budget_s=3.0):
+    """The f64 oracle as it stands on bounded samples of the other workloads,
+    each repeated for about budget_s seconds on the host cores.  GFLOP/s of
+    the sample (2 x tokens x rows x K per GEMM); a reported baseline beside
+    the GPU figures, never a target."""
+    from oracle import blr as oblr
+    from oracle import tq2 as otq2
+
+    def timed(fn, flops, sample):
+        n, c0, t0 = 0, os.times(), time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        c1 = os.times()
+        cpu = (c1.user - c0.user) + (c1.system - c0.system)
+        return dict(gflops=flops * n / dt / 1e9, cores=max(1, round(cpu / dt)), kind="oracle",
+                    sample=f"{n} x {sample} in {dt:.1f} s; cpu/wall {cpu / dt:.2f}")
+
+    res = {}
+    # skinny M=8 and the large GEMM: weight rows and tokens sampled, K and the
+    # distributions of the workload kept; each pass parses and dequantizes the
+    # sampled rows and multiplies in f64
+    for name, cfg, M, rows in (("tq2_skinny_M8", synth.SKINNY, 8, 1024), ("tq2_large", synth.LARGE, 512, 512)):
+        K = cfg["K"]
+        aos = synth.random_tq2(rows, K, cfg["wkey"])
+        x = synth.random_x(M, K, cfg["xkey"])
+        res[name] = timed(lambda: otq2.gemm(x, otq2.dequant_aos(aos, rows, K)), 2.0 * M * rows * K,
+                          f"{M} tokens x {rows} of N={cfg['N']} rows, K={K}")
+    # blr: forward + backward of one path on a token sample of C5 (4 GEMMs)
+    c = synth.BLR
+    T = 128
+    p = synth.blr_inputs(T, c["d_in"], c["d_out"], c["r"], c["key"])
+
+    def blr_step():
+        oblr.forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"])
+        oblr.backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"], p["dy"])
+    # the oracle's backward recomputes the forward: 3 forward-sized GEMM pairs per step
+    res["blr_fwd_bwd"] = timed(blr_step, 6 * 2.0 * T * c["r"] * (c["d_in"] + c["d_out"]) / 2,
+                               f"forward + backward, T={T} of {c['T']} tokens, d_in=d_out={c['d_in']}, r={c['r']}")
+    return res
+
+
 # ------------------------------------------------------------------ main ----
 def main():
     args = parse()
@@ -473,6 +518,11 @@ def main():
     if rank != 0:
         return
     cb = oracle_gemv_sample(budget_s=12.0) if world == 1 else None
+    if world == 1 and not args.no_extra:
+        try:
+            extra["oracle_cpu_samples"] = oracle_samples()
+        except Exception as e:                    # a reported baseline only: never fail the bench on it
+            extra["oracle_cpu_samples"] = {"error": f"{type(e).__name__}: {e}"}
     line = dict(
         metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
         value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,

@@ -90,3 +90,11 @@ def test_reference_arm_rank0_prints_one_line():
     assert d["value"] > 0 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_samples_report_every_workload():
+    import bench
+    r = bench.oracle_samples(budget_s=0.05)
+    assert set(r) == {"tq2_skinny_M8", "tq2_large", "blr_fwd_bwd"}
+    for v in r.values():
+        assert v["kind"] == "oracle" and v["gflops"] > 0 and v["cores"] >= 1 and v["sample"]
