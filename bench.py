@@ -144,6 +144,16 @@ def gemv_bytes(N, K):
     return N * K // 4 + N * (K // 128) * 2
 
 
+def workload_config():
+    """The workload both arms measure (the fields that do not depend on the arm)."""
+    N, K = synth.GEMV["N"], synth.GEMV["K"]
+    return {"workload": "tq2_gemv M=1 N=4096 K=4096", "gemvs_per_step": GEMV_COPIES,
+            "weights": "packed BlockTQ2_0_g128, 2 bits + f16 scale per 128",
+            "l2": f"inputs larger than L2: {GEMV_COPIES} distinct weight copies "
+                  f"({GEMV_COPIES * gemv_bytes(N, K) / 1e6:.0f} MB) rotated every step",
+            "value": "packed-weight bytes per GEMV x GEMVs / seconds"}
+
+
 def max_over_ranks(torch, dist, secs, device):
     """The job ends when its slowest rank does: every rank gets the maximum of
     the ranks' timed-region seconds (unchanged without a process group)."""
@@ -442,7 +452,6 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg_name = "tq2_gemv M=1 N=4096 K=4096"
 
     if args.impl == "reference":
         if rank != 0:
@@ -451,7 +460,10 @@ def main():
         line = dict(metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
                     value=cb["value"], unit="GB/s", impl="reference", n_gpus=args.gpus, steps=args.steps,
                     warmup=args.warmup, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
-                    data="synthetic", config={"workload": cfg_name, "weights": "packed BlockTQ2_0_g128"},
+                    data="synthetic",
+                    config=dict(workload_config(), launch="the f64 oracle, one GEMV at a time on the host cores",
+                                l2="host memory: each GEMV parses and dequantizes its weight afresh",
+                                parallelism="host cores"),
                     cpu_baseline=cb, e2e={"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                                           "d2h_bytes_per_step": 0})
         print(json.dumps(line), flush=True)
@@ -528,14 +540,9 @@ def main():
         value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=secs / args.steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="f32", data="synthetic",
-        config={"workload": cfg_name, "gemvs_per_step": GEMV_COPIES,
-                "launch": "one tq2_gemm_grouped call per step (64 jobs, shared x)",
-                "l2": f"inputs larger than L2: {GEMV_COPIES} distinct weight copies "
-                      f"({GEMV_COPIES * wbytes / 1e6:.0f} MB) rotated every step",
-                "weights": "packed BlockTQ2_0_g128, 2 bits + f16 scale per 128",
-                "activations": "f32 (split to two f16 terms on the GPU), f32 accumulation",
-                "value": "packed-weight bytes per GEMV x GEMVs / device seconds",
-                "parallelism": "replicas" if world > 1 else "single GPU"},
+        config=dict(workload_config(), launch="one tq2_gemm_grouped call per step (64 jobs, shared x)",
+                    activations="f32 (split to two f16 terms on the GPU), f32 accumulation",
+                    parallelism="replicas" if world > 1 else "single GPU"),
         tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
         roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                   "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv_grouped"),
