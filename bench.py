@@ -191,7 +191,10 @@ def run_gemv(torch, bpw, args, stream, dev):
     aos = synth.random_tq2(N, K, cfg["wkey"])
     ws = [bpw.tq2_upload(aos, N, K) for _ in range(GEMV_COPIES)]
     x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
-    outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in ws]
+    # the 64 outputs are views of one [64][M][N] buffer, so that a caller can
+    # read every result back with one copy
+    obuf = torch.empty((len(ws), M, N), dtype=torch.float32, device=dev)
+    outs = list(obuf.unbind(0))
     xs = [x] * len(ws)
 
     def grouped():
@@ -199,7 +202,7 @@ def run_gemv(torch, bpw, args, stream, dev):
 
     g = capture(torch, grouped, stream, args.warmup)
     clocks = Clocks(dev.index if dev.index is not None else 0)
-    return dict(ws=ws, x=x, xs=xs, outs=outs, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
+    return dict(ws=ws, x=x, xs=xs, outs=outs, obuf=obuf, graph=g, clocks=clocks, M=M, N=N, K=K, aos=aos)
 
 
 def extra_chained(torch, bpw, ctx, stream, pk):
@@ -221,19 +224,19 @@ def extra_chained(torch, bpw, ctx, stream, pk):
 
 def e2e_gemv(torch, bpw, ctx, stream, reps):
     """Public API with host buffers, every step: pinned x -> device, one
-    tq2_gemm_grouped call over the 64 weights, the 64 outputs -> pinned host."""
+    tq2_gemm_grouped call over the 64 weights, the 64 outputs (one [64][M][N]
+    device buffer) -> pinned host in one copy."""
     M, N, K = ctx["M"], ctx["N"], ctx["K"]
-    ws, xs, outs = ctx["ws"], ctx["xs"], ctx["outs"]
+    ws, xs, outs, obuf = ctx["ws"], ctx["xs"], ctx["outs"], ctx["obuf"]
     xh = torch.from_numpy(synth.random_x(M, K, synth.GEMV["xkey"])).pin_memory()
-    ohs = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in ws]
+    oh = torch.empty(tuple(obuf.shape), dtype=torch.float32).pin_memory()
     xd = xs[0]
 
     def step():
         with torch.cuda.stream(stream):
             xd.copy_(xh, non_blocking=True)
             bpw.tq2_gemm_grouped(ws, xs, outs, stream=stream.cuda_stream)
-            for oh, od in zip(ohs, outs):
-                oh.copy_(od, non_blocking=True)
+            oh.copy_(obuf, non_blocking=True)
         stream.synchronize()
     for _ in range(3):
         step()
