@@ -449,6 +449,30 @@ def oracle_samples(budget_s=3.0):
     return res
 
 
+METRIC = "TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline"
+
+
+def headline_line(world, steps, warmup, secs, value, gemvs, achieved, alg, pk, cb, e2e, clk, extra):
+    """The one JSON line of the default arm (the contract the driver parses).
+    secs: the slowest rank's timed seconds; value: whole-job GB/s; gemvs: per
+    rank; achieved: algorithmic GB/s of one launch."""
+    M, N, K = synth.GEMV["M"], synth.GEMV["N"], synth.GEMV["K"]
+    return dict(
+        metric=METRIC, value=value, unit="GB/s", n_gpus=world, steps=steps, warmup=warmup,
+        ms_per_step=secs / steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="f32", data="synthetic",
+        config=dict(workload_config(), launch="one tq2_gemm_grouped call per step (64 jobs, shared x)",
+                    activations="f32 (split to two f16 terms on the GPU), f32 accumulation",
+                    parallelism="replicas" if world > 1 else "single GPU"),
+        tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
+        roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                  "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv_grouped"),
+                  "kernel": "tq2_gemv_kernel<1, row-split, 64 jobs> (one launch per step)",
+                  "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"] + " hbm_gbs (copy)"},
+        cpu_baseline=cb, e2e=e2e, gpu_launches=steps, clocks=clk, extra=extra,
+    )
+
+
 # ------------------------------------------------------------------ main ----
 def main():
     args = parse()
@@ -460,7 +484,7 @@ def main():
         if rank != 0:
             return
         cb = oracle_gemv_sample(budget_s=max(3.0, min(60.0, 0.5 * (args.steps + args.warmup))))
-        line = dict(metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
+        line = dict(metric=METRIC,
                     value=cb["value"], unit="GB/s", impl="reference", n_gpus=args.gpus, steps=args.steps,
                     warmup=args.warmup, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                     data="synthetic",
@@ -538,21 +562,8 @@ def main():
             extra["oracle_cpu_samples"] = oracle_samples()
         except Exception as e:                    # a reported baseline only: never fail the bench on it
             extra["oracle_cpu_samples"] = {"error": f"{type(e).__name__}: {e}"}
-    line = dict(
-        metric="TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline",
-        value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
-        ms_per_step=secs / args.steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype="f32", data="synthetic",
-        config=dict(workload_config(), launch="one tq2_gemm_grouped call per step (64 jobs, shared x)",
-                    activations="f32 (split to two f16 terms on the GPU), f32 accumulation",
-                    parallelism="replicas" if world > 1 else "single GPU"),
-        tflops=2.0 * M * N * K * gemvs * world / secs / 1e12,
-        roofline={"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                  "frac": achieved / pk["hbm"], "traffic": profiled_traffic("tq2_gemv_grouped"),
-                  "kernel": "tq2_gemv_kernel<1, row-split, 64 jobs> (one launch per step)",
-                  "algorithmic_bytes_per_launch": alg, "peak_source": pk["src"] + " hbm_gbs (copy)"},
-        cpu_baseline=cb, e2e=e2e, gpu_launches=args.steps, clocks=clk, extra=extra,
-    )
+    line = headline_line(world=world, steps=args.steps, warmup=args.warmup, secs=secs, value=value,
+                         gemvs=gemvs, achieved=achieved, alg=alg, pk=pk, cb=cb, e2e=e2e, clk=clk, extra=extra)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -98,3 +98,34 @@ def test_oracle_samples_report_every_workload():
     assert set(r) == {"tq2_skinny_M8", "tq2_large", "blr_fwd_bwd"}
     for v in r.values():
         assert v["kind"] == "oracle" and v["gflops"] > 0 and v["cores"] >= 1 and v["sample"]
+
+
+def test_headline_line_keeps_the_contract():
+    import bench
+    pk = bench.peaks()
+    secs, steps, world = 1.7, 20000, 1
+    gemvs = steps * bench.GEMV_COPIES
+    wb = bench.gemv_bytes(4096, 4096)
+    alg = bench.GEMV_COPIES * (wb + 4 * 4096 * 2)
+    line = bench.headline_line(world=world, steps=steps, warmup=5, secs=secs,
+                               value=bench.job_gbs(wb, gemvs, world, secs), gemvs=gemvs,
+                               achieved=alg / (secs / steps) / 1e9, alg=alg, pk=pk,
+                               cb={"value": 0.04, "unit": "GB/s", "cores": 8, "kind": "oracle", "sample": "s"},
+                               e2e={"value": 1.0, "unit": "GB/s", "h2d_bytes_per_step": 16384,
+                                    "d2h_bytes_per_step": 1048576},
+                               clk={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, extra={})
+    s = json.dumps(line)                                       # serialisable as one line
+    assert "\n" not in s
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+              "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None and line["n_gpus"] == 1
+    assert line["ms_per_step"] == pytest.approx(secs / steps * 1e3)
+    assert line["config"]["workload"] == bench.workload_config()["workload"]
+    rf = line["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] == pk["hbm"]
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"])
+    assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+    assert line["gpu_launches"] == steps
