@@ -229,3 +229,106 @@ def test_quantize_scale_outside_the_f16_range():
     assert int(d_bits[0, 1]) == 0x0000 or int(d_bits[0, 1]) == 0x0001
     # 3e-8 lies between 2^-25 (the midpoint of 0 and the smallest subnormal 2^-24) and 2^-24: rounds up
     assert int(d_bits[0, 1]) == 0x0001
+
+
+# ---- pins of pack_aos (the inverse of the page's block layout) -------------
+
+def test_pack_aos_bytes_equal_the_page_packing_loop():
+    # several rows and blocks of LCG codes; every block must come out byte for
+    # byte as the page's loop packs it ({qs, d} with qs[j] = c0|c1<<2|c2<<4|c3<<6)
+    N, K = 3, 384
+    codes = synth.lcg_codes(N * K, 0x2468ACE1).reshape(N, K)
+    d_bits = np.array([[0x3C00, 0x2E66, 0xB800], [0x0001, 0x7BFF, 0x8000], [0x1234, 0x4321, 0xFC00]],
+                      dtype=np.uint16)
+    want = b"".join(_page_pack_block(codes[n, 128 * b:128 * (b + 1)], int(d_bits[n, b]))
+                    for n in range(N) for b in range(K // 128))
+    assert tq2.pack_aos(codes, d_bits) == want
+
+
+def test_pack_aos_one_hot_byte_positions():
+    # all codes 0 except code v at element e: only byte e//4 is nonzero and it
+    # holds v << 2*(e%4); the scale follows as two little-endian bytes
+    for v in (1, 2, 3):
+        for e in (0, 1, 2, 3, 4, 37, 126, 127):
+            codes = np.zeros((1, 128), dtype=np.uint8)
+            codes[0, e] = v
+            blk = tq2.pack_aos(codes, np.array([[0xABCD]], dtype=np.uint16))
+            assert len(blk) == 34
+            want = bytearray(34)
+            want[e // 4] = v << (2 * (e % 4))
+            want[32], want[33] = 0xCD, 0xAB
+            assert blk == bytes(want), (v, e)
+
+
+def test_pack_aos_literal_block():
+    # codes 0,1,2,3 repeating: every qs byte is 0 | 1<<2 | 2<<4 | 3<<6 = 0xE4
+    codes = np.tile(np.array([0, 1, 2, 3], dtype=np.uint8), 32).reshape(1, 128)
+    assert tq2.pack_aos(codes, np.array([[0x3C00]], dtype=np.uint16)) == bytes([0xE4] * 32 + [0x00, 0x3C])
+    # all codes 1 (weight 0): 0b01010101 = 0x55
+    ones = np.ones((1, 128), dtype=np.uint8)
+    assert tq2.pack_aos(ones, np.array([[0x0102]], dtype=np.uint16)) == bytes([0x55] * 32 + [0x02, 0x01])
+
+
+def test_pack_then_parse_round_trips_including_code_3():
+    rng = np.random.default_rng(7)
+    N, K = 5, 512
+    codes = rng.integers(0, 4, size=(N, K)).astype(np.uint8)          # code 3 included
+    d_bits = rng.integers(0, 1 << 16, size=(N, K // 128)).astype(np.uint16)
+    c2, d2 = tq2.parse_aos(tq2.pack_aos(codes, d_bits), N, K)
+    assert np.array_equal(c2, codes) and np.array_equal(d2, d_bits)
+    assert 3 in set(np.unique(codes))
+
+
+# ---- pins of gemm_abs (the scale of the tensor-path bound) -----------------
+
+def test_gemm_abs_hand_computed():
+    # x = [1, -2, 0.5, -4], W rows [1, 1, -1, 0] and [-0.5, 2, 2, -1]:
+    #   row 0: |1*1| + |-2*1| + |0.5*-1| + |-4*0| = 1 + 2 + 0.5 + 0 = 3.5
+    #   row 1: |1*-0.5| + |-2*2| + |0.5*2| + |-4*-1| = 0.5 + 4 + 1 + 4 = 9.5
+    # while the signed sums are 1 - 2 - 0.5 = -1.5 and -0.5 - 4 + 1 + 4 = 0.5
+    x = np.array([[1.0, -2.0, 0.5, -4.0]])
+    W = np.array([[1.0, 1.0, -1.0, 0.0], [-0.5, 2.0, 2.0, -1.0]])
+    assert np.array_equal(tq2.gemm_abs(x, W), np.array([[3.5, 9.5]]))
+    assert np.array_equal(tq2.gemm(x, W), np.array([[-1.5, 0.5]]))
+
+
+def test_gemm_abs_bounds_the_signed_sum_with_equality_for_one_sign():
+    N, K, M = 6, 256, 3
+    W = tq2.dequant_aos(synth.random_tq2(N, K, 60), N, K)
+    x = synth.random_x(M, K, 61).astype(np.float64)
+    s, a = tq2.gemm(x, W), tq2.gemm_abs(x, W)
+    assert np.all(np.abs(s) <= a * (1 + 1e-15))
+    assert np.all(a > np.abs(s))                    # mixed signs: strictly larger
+    # same-sign products: the absolute sum equals |signed sum|
+    xp, Wp = np.abs(x), np.abs(W)
+    np.testing.assert_allclose(tq2.gemm_abs(xp, Wp), tq2.gemm(xp, Wp), rtol=1e-13)
+    np.testing.assert_allclose(tq2.gemm_abs(-xp, Wp), -tq2.gemm(-xp, Wp), rtol=1e-13)
+
+
+def test_gemm_abs_ignores_signs_and_is_homogeneous():
+    N, K, M = 4, 256, 2
+    codes, d_bits = tq2.parse_aos(synth.random_tq2(N, K, 62), N, K)
+    W = tq2.dequant(codes, d_bits)
+    x = synth.random_x(M, K, 63).astype(np.float64)
+    a = tq2.gemm_abs(x, W)
+    flip = np.where(np.arange(K) % 3 == 0, -1.0, 1.0)
+    np.testing.assert_allclose(tq2.gemm_abs(x * flip, W), a, rtol=1e-13)
+    np.testing.assert_allclose(tq2.gemm_abs(x, -W), a, rtol=1e-13)
+    np.testing.assert_allclose(tq2.gemm_abs(-3.0 * x, W), 3.0 * a, rtol=1e-13)
+    # zero weights (code 1) contribute nothing: all-code-1 rows give exactly 0
+    assert np.array_equal(tq2.gemm_abs(x, np.zeros((2, K))), np.zeros((M, 2)))
+
+
+def test_gemm_abs_brute_force_tiny():
+    # a pure-Python loop over every (m, n, k) on a 2 x 128 x 3 problem
+    N, K, M = 3, 128, 2
+    W = tq2.dequant_aos(synth.random_tq2(N, K, 64), N, K)
+    x = synth.random_x(M, K, 65).astype(np.float64)
+    got = tq2.gemm_abs(x, W)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                p = x[m, k] * W[n, k]
+                acc += p if p >= 0 else -p
+            assert abs(got[m, n] - acc) <= 1e-12 * max(1.0, acc)
