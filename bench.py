@@ -37,6 +37,13 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 GEMV_COPIES = 64
+# timed replays of each secondary workload: None keeps each workload's own
+# count; --extra-reps sets one count for all (e.g. 1 for a profiler's launch list)
+EXTRA_REPS = None
+
+
+def reps(n):
+    return n if EXTRA_REPS is None else EXTRA_REPS
 
 
 def parse():
@@ -47,6 +54,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     p.add_argument("--only", default="", help="comma list of extra workloads to run")
+    p.add_argument("--extra-reps", type=int, default=None,
+                   help="timed replays of every secondary workload (default: each workload's own count)")
+    p.add_argument("--oracle-job", default="", help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -214,8 +224,9 @@ def extra_chained(torch, bpw, ctx, stream, pk):
     def step():
         for w in ws:
             bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
-    secs, _ = time_graph(torch, step, 200, 5, stream)
-    t = secs / 200 / len(ws)
+    n = reps(200)
+    secs, _ = time_graph(torch, step, n, 5, stream)
+    t = secs / n / len(ws)
     alg = gemv_bytes(N, K) + M * K * 4 + M * N * 4
     return dict(us_per_gemv=t * 1e6, gemvs_per_step=len(ws), weight_gbs=gemv_bytes(N, K) / t / 1e9,
                 alg_gbs=alg / t / 1e9, hbm_frac=alg / t / 1e9 / pk["hbm"],
@@ -263,8 +274,9 @@ def extra_skinny(torch, bpw, stream, dev, pk, Ms):
         def step():
             for w in ws:
                 bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
-        secs, _ = time_graph(torch, step, 20, 3, stream)
-        t = secs / (20 * copies)
+        n = reps(20)
+        secs, _ = time_graph(torch, step, n, 3, stream)
+        t = secs / (n * copies)
         wb = gemv_bytes(N, K)
         alg = wb + M * K * 4 + M * N * 4
         flops = 2.0 * M * N * K
@@ -306,11 +318,12 @@ def extra_blr(torch, bpw, stream, dev, pk):
 
     def sgn():
         bpw.blr_sign_grads(bu, d["h"], d["l"], d["g"], d["x"], d["dy"], a, gu, gv, stream=stream.cuda_stream)
-    tf, _ = time_graph(torch, fwd, 20, 3, stream)
-    tb, _ = time_graph(torch, bwd, 20, 3, stream)
-    ts, _ = time_graph(torch, step, 20, 3, stream)
-    tg, _ = time_graph(torch, sgn, 20, 3, stream)
-    tf, tb, ts, tg = tf / 20, tb / 20, ts / 20, tg / 20
+    n = reps(20)
+    tf, _ = time_graph(torch, fwd, n, 3, stream)
+    tb, _ = time_graph(torch, bwd, n, 3, stream)
+    ts, _ = time_graph(torch, step, n, 3, stream)
+    tg, _ = time_graph(torch, sgn, n, 3, stream)
+    tf, tb, ts, tg = tf / n, tb / n, ts / n, tg / n
     sflops = 3 * 2.0 * T * dout * r                     # b, G_U and G_V: three GEMMs of 2*T*4096*512
     flops = 4 * 2.0 * T * din * r                       # four GEMMs of 2*T*4096*512 (c recomputed: a fifth)
     alg_bytes = 5 * T * din * 4 + 2 * dout * r // 8 + 2 * T * r * 4
@@ -332,8 +345,9 @@ def extra_large(torch, bpw, stream, dev, pk):
 
     def step():
         bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
-    secs, _ = time_graph(torch, step, 10, 3, stream)
-    t = secs / 10
+    n = reps(10)
+    secs, _ = time_graph(torch, step, n, 3, stream)
+    t = secs / n
     flops = 2.0 * M * N * K
     tfl = flops / t / 1e12
     w.free()
@@ -353,8 +367,9 @@ def extra_dit(torch, bpw, stream, dev, pk):
 
         def step():
             bpw.tq2_gemm(w, x, out, stream=stream.cuda_stream)
-        secs, _ = time_graph(torch, step, 10, 3, stream)
-        t = secs / 10
+        n = reps(10)
+        secs, _ = time_graph(torch, step, n, 3, stream)
+        t = secs / n
         tfl = 2.0 * M * N * K / t / 1e12
         w.free()
         res[f"M{M}_N{N}_K{K}"] = dict(us=t * 1e6, tflops=tfl, tensor_frac=tfl / pk["bf16"],
@@ -373,8 +388,9 @@ def extra_quantize(torch, bpw, stream, dev, pk):
 
     def step():
         bpw.tq2_quantize(W, aos, stream=stream.cuda_stream)
-    secs, _ = time_graph(torch, step, 20, 3, stream)
-    t = secs / 20
+    n = reps(20)
+    secs, _ = time_graph(torch, step, n, 3, stream)
+    t = secs / n
     nbytes = N * K * 4 + N * (K // 128) * 34
     return dict(us=t * 1e6, alg_gbs=nbytes / t / 1e9, hbm_frac=nbytes / t / 1e9 / pk["hbm"], bound="hbm",
                 algorithmic_bytes=nbytes, workload=f"f32 W [{N}][{K}] -> BlockTQ2_0_g128")
@@ -449,6 +465,80 @@ def oracle_samples(budget_s=3.0):
     return res
 
 
+def _oracle_job(name):
+    """One full-size run of the f64 oracle (called in a child process whose BLAS
+    thread count the parent fixes); returns (seconds, cpu seconds, flops,
+    sample) of the oracle's work, input generation excluded."""
+    from oracle import blr as oblr
+    from oracle import tq2 as otq2
+
+    def clock():
+        c = os.times()
+        return time.perf_counter(), c.user + c.system
+    t0, c0 = clock()
+    if name == "tq2_tiny_C1":
+        aos, N, K, xs = synth.tiny_tq2(M_list=(1, 7, 8, 9, 100))
+        W = otq2.dequant_aos(aos, N, K)
+        for x in xs.values():
+            otq2.gemm(x, W)
+        flops = sum(2.0 * M * N * K for M in xs)
+        sample = f"N={N} K={K}, M in 1,7,8,9,100 (AoS parse + f64 dequant + f64 GEMM)"
+    elif name in ("tq2_gemv_C2", "tq2_skinny_M8_C3", "tq2_large_C4"):
+        cfg, M = {"tq2_gemv_C2": (synth.GEMV, 1), "tq2_skinny_M8_C3": (synth.SKINNY, 8),
+                  "tq2_large_C4": (synth.LARGE, synth.LARGE["M"])}[name]
+        N, K = cfg["N"], cfg["K"]
+        aos = synth.random_tq2(N, K, cfg["wkey"])
+        x = synth.random_x(M, K, cfg["xkey"])
+        t0, c0 = clock()                                  # input generation is not the oracle's work
+        otq2.gemm(x, otq2.dequant_aos(aos, N, K))
+        flops = 2.0 * M * N * K
+        sample = f"full M={M} N={N} K={K} (AoS parse + f64 dequant + f64 GEMM)"
+    elif name == "blr_C5":
+        c = synth.BLR
+        p = synth.blr_inputs(c["T"], c["d_in"], c["d_out"], c["r"], c["key"])
+        t0, c0 = clock()
+        oblr.forward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"])
+        oblr.backward(p["bits_u"], p["bits_v"], p["h"], p["l"], p["g"], p["x"], p["dy"])
+        # forward: 2 GEMMs; the oracle's backward recomputes a and c: 4 more
+        flops = 6 * 2.0 * c["T"] * c["r"] * c["d_in"]
+        sample = f"full forward + backward T={c['T']} d_in=d_out={c['d_in']} r={c['r']}"
+    else:
+        raise ValueError(name)
+    t1, c1 = clock()
+    return t1 - t0, c1 - c0, flops, sample
+
+
+def oracle_full_runs(timeout_s=120.0):
+    """The f64 oracle as it stands on the full workloads: single-threaded on C1,
+    C2 and C3 M=8, and over all host cores on C2, C3 M=8, C4 and C5.  Each run
+    is a child process with the BLAS thread count fixed through the
+    environment; ``cores`` is its CPU time over wall time.  Reported beside the
+    GPU figures, never a target."""
+    jobs = [("tq2_tiny_C1", 1), ("tq2_gemv_C2", 1), ("tq2_skinny_M8_C3", 1),
+            ("tq2_gemv_C2", 0), ("tq2_skinny_M8_C3", 0), ("tq2_large_C4", 0), ("blr_C5", 0)]
+    res = {}
+    for name, threads in jobs:
+        env = dict(os.environ)
+        if threads:
+            for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+                env[v] = str(threads)
+        key = f"{name}_{'1thread' if threads else 'all_cores'}"
+        try:
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-job", name], env=env,
+                               capture_output=True, text=True, timeout=timeout_s)
+            res[key] = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else \
+                {"error": r.stderr.strip().splitlines()[-1:] or ["rc %d" % r.returncode]}
+        except Exception as e:                    # a reported baseline only: never fail the bench on it
+            res[key] = {"error": f"{type(e).__name__}: {e}"}
+    return res
+
+
+def oracle_job_main(name):
+    secs, cpu, flops, sample = _oracle_job(name)
+    print(json.dumps(dict(seconds=secs, gflops=flops / secs / 1e9, cores=max(1, round(cpu / secs)),
+                          cpu_over_wall=cpu / secs, kind="oracle", sample=sample, host_cores=os.cpu_count())))
+
+
 METRIC = "TQ2 GEMM TFLOP/s and weight GB/s at M=1..4096, % of GB300 roofline"
 
 
@@ -476,6 +566,11 @@ def headline_line(world, steps, warmup, secs, value, gemvs, achieved, alg, pk, c
 # ------------------------------------------------------------------ main ----
 def main():
     args = parse()
+    if args.oracle_job:
+        oracle_job_main(args.oracle_job)
+        return
+    global EXTRA_REPS
+    EXTRA_REPS = args.extra_reps
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -539,7 +634,9 @@ def main():
     e2e = e2e_gemv(torch, bpw, ctx, stream, reps=max(20, min(200, args.steps // 10)))
 
     extra = {}
-    if not args.no_extra and rank == 0:
+    # the secondary workloads run in single-GPU runs only: a multi-GPU run
+    # measures the replicated headline step and nothing else
+    if not args.no_extra and world == 1:
         only = set(filter(None, args.only.split(",")))
         if not only or "skinny" in only:
             extra["tq2_skinny_N11008"] = extra_skinny(torch, bpw, stream, dev, pk, (8, 32, 128))
@@ -562,6 +659,8 @@ def main():
             extra["oracle_cpu_samples"] = oracle_samples()
         except Exception as e:                    # a reported baseline only: never fail the bench on it
             extra["oracle_cpu_samples"] = {"error": f"{type(e).__name__}: {e}"}
+        if not args.only or "oracle_full" in args.only:
+            extra["oracle_cpu_full"] = oracle_full_runs()
     line = headline_line(world=world, steps=args.steps, warmup=args.warmup, secs=secs, value=value,
                          gemvs=gemvs, achieved=achieved, alg=alg, pk=pk, cb=cb, e2e=e2e, clk=clk, extra=extra)
     print(json.dumps(line), flush=True)

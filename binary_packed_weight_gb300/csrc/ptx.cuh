@@ -371,35 +371,4 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&o)[8]) {
     o[7] = decode_pair<6>(w8);
 }
 
-// Offset decode: pair q of a word (elements q and q+8, at bits 2q and
-// 16+2q) as the exact f16 pair (m_q + c_lo, m_q + c_hi), with the code moved
-// to bit P in {4, 6, 8} of each half and OR-ed into the mantissa of
-// m_q = 2^(10-P) (64, 16 or 4).  One shift serves up to three pairs and no
-// subtraction is needed: the MMA sums (m_q + c) x and the caller removes
-// sum_k (m_q + 1) x_k, which depends on x alone, once per block.
-//   q:   0   1   2   3   4   5   6   7
-//   P:   4   6   8   4   6   8   4   6     (word shifted by <<4, >>2, >>8)
-//   m_q: 64  16  4   64  16  4   64  16
-template <int P>
-__device__ __forceinline__ uint32_t offset_pair(uint32_t ws) {
-    constexpr uint32_t mask = 0x00030003u << P;
-    constexpr uint32_t mh = (uint32_t)(25 - P) << 10;     // f16 bits of 2^(10-P)
-    return (ws & mask) | (mh | (mh << 16));
-}
-__device__ __forceinline__ void decode_word_offset(uint32_t w, uint32_t (&o)[8]) {
-    const uint32_t a = w << 4, b = w >> 2, c = w >> 8;
-    o[0] = offset_pair<4>(a);
-    o[1] = offset_pair<6>(a);
-    o[2] = offset_pair<8>(a);
-    o[3] = offset_pair<4>(b);
-    o[4] = offset_pair<6>(b);
-    o[5] = offset_pair<8>(b);
-    o[6] = offset_pair<4>(c);
-    o[7] = offset_pair<6>(c);
-}
-// m_q + 1 for the element at position e (0..15) of a word.
-__host__ __device__ constexpr float offset_plus_one(int e) {
-    return (e % 8 == 2 || e % 8 == 5) ? 5.f : ((e % 8 == 1 || e % 8 == 4 || e % 8 == 7) ? 17.f : 65.f);
-}
-
 }  // namespace tq2

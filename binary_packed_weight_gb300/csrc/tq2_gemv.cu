@@ -20,7 +20,10 @@
 //     shared memory, then per stage decode their 4 blocks (shift +
 //     mask|magic, see gv_pair) and issue the MMAs: one accumulator chain
 //     per block, four interleaved per warp, f32 accumulate, block scale
-//     applied to the block result d * (acc - correction).
+//     applied to the block result d * (acc - correction).  The correction
+//     sum_k (m_q+1) x_k of a block is computed by the very MMA chain that a
+//     block of all code-1 weights takes, so such a block gives exactly 0 and
+//     the rounding error of a block scales with its nonzero weights.
 //   * Two ways to cut the work (the smem addressing of a warp's share is the
 //     same in both):
 //       k-split (small N): a unit is 16 rows; a stage covers them over 32
@@ -129,11 +132,6 @@ __device__ __forceinline__ uint32_t gv_pair(uint32_t w, uint32_t wl, uint32_t wr
     else if constexpr (Q == 6) return gv_op<6>(wr, sh.k6);
     else return gv_op<8>(wr, sh.k8);
 }
-// m_q + 1 for the element at position e (0..15) of a word.
-__host__ __device__ constexpr float gv_plus_one(int e) {
-    return (e % 8 == 4 || e % 8 == 7) ? 5.f : ((e % 8 == 1 || e % 8 == 3 || e % 8 == 6) ? 17.f : 65.f);
-}
-
 // The A fragment of k16 step j (0..3) of a word: rows g and g+8 from words
 // wa and wb; positions 2t,2t+1 hold pair 2j, positions 2t+8,2t+9 pair 2j+1.
 template <int J>
@@ -371,6 +369,22 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
     }
     auto consumers_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(GV_CONS * 32) : "memory"); };
 
+    // this lane's x fragments (uint4 units); lanes g >= 2MT alias column g % 2MT
+    const int xstep = 4 * (2 * MT) * 4, sstep = (2 * MT) * 4;
+    const uint4* xl = reinterpret_cast<const uint4*>(xs) + (g % (2 * MT)) * 4 + t;
+    const uint32_t z = (uint32_t)(K >> 30);      // 0 (K < 2^30), opaque to the compiler
+    const GvShift sh{16u | z, (1u << 26) | z, 0x00300030u | z, 0x00C000C0u | z, 0x03000300u | z};
+    // A fragments of a word whose 16 codes are all 1 (weight 0), k16 steps 0..3
+    uint32_t ones[4][4];
+    {
+        uint32_t w1[3];
+        gv_word(0x55555555u | z, sh, w1);
+        gv_afrag<0>(w1, w1, ones[0], sh);
+        gv_afrag<1>(w1, w1, ones[1], sh);
+        gv_afrag<2>(w1, w1, ones[2], sh);
+        gv_afrag<3>(w1, w1, ones[3], sh);
+    }
+
     pdl_wait();
     const float* staged = nullptr;
     auto stage_x = [&](const float* x) {
@@ -390,9 +404,6 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
                     const float4 q = live ? __ldg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                     e[4 * v] = q.x; e[4 * v + 1] = q.y; e[4 * v + 2] = q.z; e[4 * v + 3] = q.w;
                 }
-                float cs = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) cs = fmaf(gv_plus_one(i), e[i], cs);
                 if (live) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {               // k16 step 4y + j: pairs 2j, 2j+1
@@ -405,23 +416,31 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
                         d[8] = make_uint2(l01, l23);              // column 2m+1: lo
                     }
                 }
-                cs += __shfl_xor_sync(0xffffffffu, cs, 1);
-                cs += __shfl_xor_sync(0xffffffffu, cs, 2);
-                cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-                if (live && (lane & 7) == 0) corr[blk * MT + m] = cs;
             }
         }
         if (MODE == GV_ROWS) consumers_sync();                // every block converted
         else __syncwarp();
+        // Corrections sum_k (m_q+1) x_k per block and token: the MMA chain of
+        // gv_piece (same steps, same order, accumulator from zero) on a row of
+        // all code-1 weights, so that d * (acc - correction) is exactly 0 for
+        // such a block.  Each warp takes the blocks it staged.
+        for (int li = 0; li < nbw; ++li) {
+            const int blk = MODE == GV_KSPLIT ? (li / GV_BPW) * (GV_BPW * GV_CONS) + GV_BPW * warp + li % GV_BPW
+                                              : warp + GV_CONS * li;
+            const uint4* xb = xl + blk * xstep;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint4 b = xb[p * sstep];
+                mma_16816_pure(acc, ones[(2 * p) & 3], b.x, b.y);
+                mma_16816_pure(acc, ones[(2 * p + 1) & 3], b.z, b.w);
+            }
+            if (g == 0 && t < MT) corr[blk * MT + t] = acc[0] + acc[1];
+        }
+        if (MODE == GV_ROWS) consumers_sync();                // every correction written
+        else __syncwarp();
         staged = x;
     };
-
-    // this lane's x fragments: column g < 2MT, else the zero area
-    // this lane's x fragments (uint4 units); lanes g >= 2MT alias column g % 2MT
-    const int xstep = 4 * (2 * MT) * 4, sstep = (2 * MT) * 4;
-    const uint4* xl = reinterpret_cast<const uint4*>(xs) + (g % (2 * MT)) * 4 + t;
-    const uint32_t z = (uint32_t)(K >> 30);      // 0 (K < 2^30), opaque to the compiler
-    const GvShift sh{16u | z, (1u << 26) | z, 0x00300030u | z, 0x00C000C0u | z, 0x03000300u | z};
 
     int s = 0, slot = 0, job = 0;
     uint32_t ph = 0, sph = 0;

@@ -12,9 +12,9 @@
 // Skinny GEMM: out[m,n] = sum_k x[m,k] W[n,k] for M <= 16 with f32
 // activations.  The contraction runs on mma.sync m16n8k16 (f16 in, f32
 // accumulate) because at M <= 16 the kernel is bound by issue slots: one
-// HMMA replaces 2*M FFMAs per weight per thread.  Each x is split exactly
-// enough into hi = f16(x) and lo = f16(x - hi) (two B columns), which leaves
-// a relative residual below 2^-21.  Weights enter the MMA as (c-1) in f16
+// HMMA replaces 2*M FFMAs per weight per thread.  Each x is carried as
+// hi = f16(x) and lo = f16(x - hi) (two B columns); hi + lo differs from x by
+// a relative residual of about 2^-22.  Weights enter the MMA as (c-1) in f16
 // (exact); the block scale d multiplies the f32 block partial afterwards.
 #include <mutex>
 
@@ -319,7 +319,10 @@ std::mutex g_static_scratch_mutex;
 
 // Device address of g_static_scratch on the current device, looked up once
 // per device (host code only sees a stand-in for the array, never its device
-// address, so the address must come from cudaGetSymbolAddress).
+// address, so the address must come from cudaGetSymbolAddress).  The cache
+// assumes that the device's primary context lives as long as the process:
+// after cudaDeviceReset the cached address is stale, so a process that resets
+// a device must not call tq2_gemm_skinny_static on it again.
 cudaError_t static_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -356,6 +359,12 @@ extern "C" TQ2_API tq2_status tq2_gemm_skinny_static(tq2_handle h, const float* 
                                      "tq2_gemm_skinny_static: needs %zu bytes of scratch for M=%lld K=%lld, above the "
                                      "fixed %zu-byte area (ceil(M/4)*K*16 must be <= %zu)",
                                      need, (long long)M, (long long)K, kStaticScratchBytes, kStaticScratchBytes);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
+        return (tq2_status)tq2::set_error(TQ2_EINVAL,
+                                          "tq2_gemm_skinny_static: the handle lives on device %d but device %d is "
+                                          "current (the fixed scratch array is per device)",
+                                          h->device, dev);
     void* scratch = nullptr;
     cudaError_t e = static_scratch(&scratch);
     if (e != cudaSuccess)

@@ -143,9 +143,17 @@ TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
  *           x) is taken from the stream-ordered allocator of the current
  *           device and released on the same stream.
  *
- * M <= 16 runs the skinny kernel: f32 activations split exactly into two
- * f16 terms, f32 accumulation; |error| <= 1e-3 at K <= 4096 for unit-scale
- * data.  For M <= 2 and M*K <= 32768 it is a single kernel with no scratch.
+ * M <= 16 runs the skinny kernel: each f32 activation is carried as two f16
+ * terms, hi = f16(x) and lo = f16(x - hi), whose sum differs from x by at
+ * most about 2^-22 |x| (the weights are exact), with f32 accumulation:
+ * |error| <= 2^-12 sum_k |x[m,k] W[n,k]| + 1e-7 per element, which is within
+ * the pages' 1e-3 at K <= 4096 for unit-scale data.  For M <= 2 and
+ * M*K <= 32768 it is a single kernel with no scratch; that kernel decodes
+ * codes with an offset that it removes per 128-block, so the rounding of a
+ * block that holds a nonzero weight scales with that block's sum of |x|
+ * (tested within the bound above on weights with 99 % zeros and x up to 256x
+ * unit scale).  On every path a block whose codes are all 1 contributes
+ * exactly 0, so an all-zero row gives exactly 0.
  * M > 16 runs the tensor-core kernel: activations rounded to f16
  * (nearest-even), weights exact in f16, f32 accumulation;
  * |error| <= 1e-2 * sum_k |x[m,k] W[n,k]|.
@@ -220,15 +228,20 @@ TQ2_API tq2_status tq2_quantize(const float* w, int64_t N, int64_t K, void* aos_
  * processes that reserve all device memory up front, and real-time loops in
  * which an allocator call could stall or fail.
  *
- *   Same arguments and result as tq2_gemm with M <= 16 (the skinny kernel).
+ *   Same arguments as tq2_gemm with 1 <= M <= 16; it always runs the staged
+ *   skinny kernel, so its results equal tq2_gemm's bit for bit for M >= 3 and
+ *   differ from them only by rounding for M <= 2, where tq2_gemm takes the
+ *   fused GEMV (both within the skinny bound of tq2_gemm).
+ *   The handle must live on the current device, else TQ2_EINVAL.
  *   Scratch: a fixed 1 MiB device array inside the library (one per GPU that
  *   loads it, held until the process exits) holds the staged f16 fragments
  *   of x, ceil(M/4)*K*16 bytes; larger requests (for example K > 16384 at
  *   M = 16, K > 65536 at M <= 4) return TQ2_ESHAPE.  No cudaMalloc,
  *   cudaFree or stream-ordered allocation is made.
  *   The first call on a device looks up the array's device address on the
- *   current device (cudaGetSymbolAddress) and caches it; make that first
- *   call before any stream capture.
+ *   current device (cudaGetSymbolAddress) and caches it for the life of the
+ *   process; make that first call before any stream capture, and do not call
+ *   this function on a device after resetting it (cudaDeviceReset).
  *   Every call shares the one array: calls whose work may overlap on the GPU
  *   (different streams, or different threads without ordering) race on it.
  *   Nothing in it needs clearing between calls: each call writes every byte

@@ -393,10 +393,8 @@ def test_edge_cases(lib):
             x = synth.random_x(M, K, 83)
             got = run_gemm(lib, w2, x)
             r = oracle_gemm(a2, N, K, x)
-            if code == 1 and M > 2:
-                assert np.all(got == 0.0)       # exact (c-1) decode paths
-            elif code == 1:
-                assert np.max(np.abs(got)) <= 1e-3   # offset decode: rounding noise only
+            if code == 1:
+                assert np.all(got == 0.0), M    # every path, the offset-decode GEMV included
             else:
                 (check_skinny(got, r[0], r[1]) if M <= 16 else check_tensor(got, *r))
     lib.device_status()
@@ -490,3 +488,52 @@ def test_tiny_page_against_golden(tiny, lib):
         got = run_gemm(lib, w, xs[M])
         want = load_matrix(f"tq2_page_tiny_M{M}.txt")
         assert np.abs(got - want).max() <= 1e-3, M
+
+
+# ---- accuracy of the decode-shape GEMV (offset decode) on data that is not unit-scale
+
+def _sparse_weights(N, K, key, p_nonzero, zero_rows=()):
+    """Codes mostly 1 (weight 0): each code is 0 or 2 with probability p_nonzero;
+    rows in zero_rows are all code 1.  Scales U(0.01, 0.1)."""
+    u = synth.uniform01(N * K, key).reshape(N, K)
+    c2 = synth.codes3(N * K, key + 1).reshape(N, K)
+    codes = np.where(u < p_nonzero, np.where(c2 == 0, 0, 2), 1).astype(np.uint8)
+    for r in zero_rows:
+        codes[r] = 1
+    d = synth.f16_bits(synth.uniform(N * (K // 128), key + 2, 0.01, 0.1)).reshape(N, K // 128)
+    return synth.pack_aos(codes, d), codes
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("p_nonzero", [0.1, 0.01])
+@pytest.mark.parametrize("xscale", [1.0, 16.0, 256.0])
+def test_gemv_sparse_weights_scaled_x(lib, p_nonzero, xscale):
+    """M = 1 and 2 through tq2_gemm (the fused GEMV) and tq2_gemm_grouped on
+    weights with >= 90 % zero codes, rows of all code 1 mixed with dense rows,
+    and x ~ N(0,1) times 1, 16 and 256: element by element within
+    2^-12 * sum|x W| + 1e-7 (f32 accumulation), and exactly 0 on the all-zero
+    rows.  The bound scales with the row's nonzero weights, not with x."""
+    import torch
+    zero_rows = (0, 5, 127, 128, 2000, 4095)
+    for N, K in ((4096, 4096), (300, 8192)):
+        zr = tuple(r for r in zero_rows if r < N)
+        aos, codes = _sparse_weights(N, K, 700 + int(1000 * p_nonzero), p_nonzero, zr)
+        w = lib.tq2_upload(aos, N, K)
+        W = otq2.dequant_aos(aos, N, K)
+        for M in (1, 2):
+            x = (synth.random_x(M, K, 710 + M) * np.float32(xscale)).astype(np.float32)
+            ref, absref = otq2.gemm(x, W), otq2.gemm_abs(x, W)
+            got = run_gemm(lib, w, x)
+            err = np.abs(got - ref)
+            bad = err > 2.0 ** -12 * absref + 1e-7
+            assert not bad.any(), (N, K, M, int(bad.sum()), float(err.max()))
+            assert np.all(got[:, list(zr)] == 0.0), (N, K, M)
+            # the same GEMV inside a grouped launch (row-split when the group fills the GPU)
+            outs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(40)]
+            xd = to_dev(x)
+            lib.tq2_gemm_grouped([w] * 40, [xd] * 40, outs)
+            lib.device_status()
+            for o in (outs[0], outs[39]):
+                g2 = o.cpu().numpy().astype(np.float64)
+                assert np.array_equal(g2, got), (N, K, M)
+        w.free()

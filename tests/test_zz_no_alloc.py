@@ -1,12 +1,13 @@
-"""The allocation-free skinny GEMM (tq2_gemm_skinny_static) against tq2_gemm.
+"""The allocation-free skinny GEMM (tq2_gemm_skinny_static).
 
 Callers that must not allocate device memory during a GEMM (plugin or
 custom-op interfaces that forbid allocation while enqueuing work, serving
 processes that reserve all device memory up front, real-time loops) use
 tq2_gemm_skinny_static, whose scratch is a fixed device array inside the
 library.  This test calls it through the C ABI twice in a row per shape and
-checks each result against the regular entry point within the skinny
-kernel's tolerance.  The file name makes pytest collect it last.
+checks each result against the f64 oracle within the skinny kernel's bound,
+and, for M >= 3 where tq2_gemm runs the same staged skinny kernel, for bit
+equality with tq2_gemm.  The file name makes pytest collect it last.
 """
 import ctypes
 
@@ -14,6 +15,8 @@ import numpy as np
 import pytest
 
 import synth
+from gpu_util import check_skinny
+from oracle import tq2 as otq2
 
 pytestmark = pytest.mark.gpu
 
@@ -31,16 +34,20 @@ def _run(lib, fn_name, w, x):
     return out.cpu().numpy().astype(np.float64)
 
 
-def test_static_scratch_matches_regular_entry_point(lib):
+def test_static_scratch_matches_oracle_and_regular_entry_point(lib):
     N, K = 3000, 4096
-    w = lib.tq2_upload(synth.random_tq2(N, K, 301), N, K)
-    for M in (1, 6, 16):
+    aos = synth.random_tq2(N, K, 301)
+    w = lib.tq2_upload(aos, N, K)
+    W = otq2.dequant_aos(aos, N, K)
+    for M in (1, 2, 3, 6, 16):
         x = synth.random_x(M, K, 302 + M)
-        want = _run(lib, "tq2_gemm", w, x)
-        for _ in range(2):                                  # two calls in a row
+        ref, absref = otq2.gemm(x, W), otq2.gemm_abs(x, W)
+        regular = _run(lib, "tq2_gemm", w, x)
+        for call in range(2):                               # two calls in a row
             got = _run(lib, "tq2_gemm_skinny_static", w, x)
-            assert np.all(np.isfinite(got))
-            assert np.max(np.abs(got - want)) <= 1e-3, M
+            check_skinny(got, ref, absref, f"static M={M} call {call}")
+            if M >= 3:                                      # the same kernel as tq2_gemm
+                assert np.array_equal(got, regular), M
 
 
 def test_static_scratch_refuses_oversized_requests(lib):
