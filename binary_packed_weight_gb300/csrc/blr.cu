@@ -9,18 +9,21 @@
 // Bitmap convention (kernels expand / expand_n / expand_t on that page):
 // bits [rows][r/32] u32, bit j of word w is rank 32w + j, a set bit is +1.
 //
-// GPU mapping.  Each product is one tcgen05 GEMM D[t,n] = sum_k act[t,k] P[n,k]
-// over a sign plane P decoded from bits on chip (umma_core.cuh, DecSign):
-//   a  : act = f16(x.g)            P = S_V^T  (bits of S_V transposed, [r][d_in/32]),  K = d_in
-//   c  : act = f16(a.l)            P = S_U    (bits_u as given),                        K = r
-//   b  : act = f16(dy.h.gs)        P = S_U^T  (bits of S_U transposed),                 K = d_out
-//   dx': act = f16(b.l.gs)         P = S_V    (bits_v as given),                        K = r
-// The elementwise factors are fused into the f16 staging passes (as the
-// page's cvt kernels do), y = h.c and dx = g.dx' into the GEMM epilogues, and
-// the column sums dh, dl, dg are two-pass reductions in a fixed order
-// (partials per token tile or chunk, then an ordered sum), so every result is
-// deterministic.  gs (a power of two) keeps staged gradients away from the
-// f16 subnormals; the GEMMs divide it back out.
+// GPU mapping.  The two products that contract over d_in or d_out and land
+// in rank space (a, b) run in blr_rank.cu: one pass over the f32 activation,
+// rounded to f16 on chip, times the sign plane read in its own row order,
+// reduced over a cluster in a fixed order.  The two that expand rank space
+// back to d_out or d_in (c, dx') are tcgen05 GEMMs on the core
+// (umma_core.cuh) with the sign plane decoded on chip (DecSign, the bits as
+// given) and the f16 rank-space operand staged by the rank kernel:
+//   a  : f16(x.g)        x S_V        K = d_in    (blr_rank.cu; also a_save, f16(a.l))
+//   c  : f16(a.l)        x S_U^T      K = r       (core; y = h.c in the epilogue)
+//   b  : f16(dy.h.gs)    x S_U  / gs  K = d_out   (blr_rank.cu; f16(b.l.gs), dl partials)
+//   dx': f16(b.l.gs)     x S_V^T / gs K = r       (core; dx = g.dx', dg partials)
+// The column sums dh, dl, dg are two-pass reductions in a fixed order
+// (partials per token tile or 32-token chunk, then an ordered sum), so every
+// result is deterministic.  gs (a power of two) keeps staged gradients away
+// from the f16 subnormals; the GEMMs divide it back out.
 #include <cmath>
 
 #include "../../include/tq2.h"
@@ -53,26 +56,6 @@ cudaError_t launch_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, ui
     const int64_t n = rows * r;
     expand_bits_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(bits, rows, r, plane, transpose);
     return cudaGetLastError();
-}
-
-// -------------------------------------------------------- bit transpose ----
-// bits [rows][r/32] -> out [r][rows/32]: warp per 32x32 bit tile; lane i holds
-// row 32*rg+i's word kw; the ballot over bit b gives column 32*kw+b's 32 bits.
-__global__ void bits_transpose_kernel(const uint32_t* __restrict__ bits, uint32_t* __restrict__ out, int rows,
-                                      int r) {
-    const int wpr = r / 32, opr = rows / 32;
-    const int64_t tile = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (tile >= (int64_t)opr * wpr) return;
-    const int lane = threadIdx.x & 31;
-    const int rg = (int)(tile / wpr), kw = (int)(tile % wpr);
-    const uint32_t w = bits[(int64_t)(32 * rg + lane) * wpr + kw];
-    uint32_t mine = 0;
-#pragma unroll
-    for (int b = 0; b < 32; ++b) {
-        const uint32_t m = __ballot_sync(0xffffffffu, (w >> b) & 1u);
-        if (lane == b) mine = m;
-    }
-    out[(int64_t)(32 * kw + lane) * opr + rg] = mine;
 }
 
 // ------------------------------------------------------------- staging ----
@@ -111,45 +94,8 @@ __global__ void stage32_kernel(const float* __restrict__ src, const float* __res
     }
 }
 
-// Sum of S split-K partials [S][T][r] (fixed order) times `oscale`; writes the
-// f32 result (if res) and the 32-group staged f16 of result * col * scale; and,
-// if colpart is given, colpart[chunk][k] = sum over the chunk's tokens (in
-// order) of result * other.  Block (32, 8): x = column within a 32-column
-// group, y = token lane; FIN_TC tokens per block.
+// Tokens per partial column sum (a chunk) of the colsum kernels.
 constexpr int FIN_TC = 32;
-__global__ void finish_splitk_kernel(const float* __restrict__ part, int S, int T, int r, float oscale,
-                                     float* __restrict__ res, const float* __restrict__ col, float scale,
-                                     uint16_t* __restrict__ dst16, const float* __restrict__ other,
-                                     float* __restrict__ colpart) {
-    __shared__ float red[8][33];
-    pdl_wait();
-    pdl_launch_dependents();
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int k = blockIdx.x * 32 + tx;
-    const int t0 = blockIdx.y * FIN_TC;
-    const bool kok = k < r;
-    const int pos = (k & ~31) + (tx < 16 ? 2 * tx : 2 * (tx - 16) + 1);
-    const float cs = kok ? col[k] : 0.f;
-    float acc = 0.f;
-    for (int t = t0 + ty; t < t0 + FIN_TC && t < T; t += 8) {
-        if (!kok) continue;
-        float v = 0.f;
-        for (int s = 0; s < S; ++s) v += part[((int64_t)s * T + t) * r + k];
-        v *= oscale;
-        if (res) res[(int64_t)t * r + k] = v;
-        dst16[(int64_t)t * r + pos] = __half_as_ushort(__float2half_rn(v * cs * scale));
-        if (colpart) acc = fmaf(v, other[(int64_t)t * r + k], acc);
-    }
-    if (colpart) {
-        red[ty][tx] = acc;
-        __syncthreads();
-        if (ty == 0 && kok) {
-            float s2 = 0.f;
-            for (int i = 0; i < 8; ++i) s2 += red[i][tx];
-            colpart[(int64_t)blockIdx.y * r + k] = s2;
-        }
-    }
-}
 
 // dst[c][t] = f16(src[t][c] * col[c] * scale) for t < T and 0 for T <= t < Tp:
 // an operand of a GEMM over the token axis, transposed so that the tokens
@@ -193,7 +139,8 @@ __global__ void __launch_bounds__(256) stage_t16_kernel(const float* __restrict_
 }
 
 // colpart[chunk][n] = sum over the chunk's tokens of A[t][n] * B[t][n]
-// (block (32, 8) as finish_splitk_kernel; fixed order).
+// (block (32, 8): x = column within a 32-column group, y = token lane; fixed
+// order).
 __global__ void colsum_prod_kernel(const float* __restrict__ A, const float* __restrict__ B, int T, int n,
                                    float* __restrict__ colpart) {
     __shared__ float red[8][33];
@@ -256,19 +203,12 @@ int sm_count() {
     return sms;
 }
 
-int pick_splits(int R, int T, int K, int BN) {
-    const int tiles = ((R + UM_BM - 1) / UM_BM) * ((T + BN - 1) / BN);
-    const int nk = K / UM_BK;
-    int s = (sm_count() + tiles - 1) / tiles;
-    if (s > 8) s = 8;
-    if (s > nk) s = nk;
-    return s < 1 ? 1 : s;
-}
-
-cudaError_t transpose_bits(const uint32_t* bits, uint32_t* out, int rows, int r, cudaStream_t st) {
-    const int64_t tiles = (int64_t)(rows / 32) * (r / 32);
-    bits_transpose_kernel<<<(unsigned)((tiles + 7) / 8), 256, 0, st>>>(bits, out, rows, r);
-    return cudaGetLastError();
+// Token tile of the layer's GEMMs: at most 128 tokens, so the decoded sign
+// planes stay in tensor memory (the core's AT mode) and the activation tiles
+// are the only shared-memory operand.
+int blr_bn(int T) {
+    const int bn = umma_pick_bn(T);
+    return bn > 128 ? 128 : bn;
 }
 
 cudaError_t stage32(const float* src, const float* col, float scale, void* dst, int T, int Kd, cudaStream_t st) {
@@ -283,24 +223,6 @@ cudaError_t stage32(const float* src, const float* col, float scale, void* dst, 
 cudaError_t colsum_finish(const float* colpart, int chunks, int n, float* out, cudaStream_t st) {
     return launch_pdl(colsum_finish_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, colpart, chunks, n,
                       out);
-}
-
-// a = (x.g) S_V  (split K, partials summed by finish, which also stages a.l)
-cudaError_t forward_a(const uint32_t* bits_vT, const float* x, const float* g, const float* l, float* a_save,
-                      void* al16, int T, int d_in, int r, Scratch& sc, cudaStream_t st) {
-    void* xg16 = sc.take<uint16_t>((size_t)T * d_in);
-    cudaError_t e = stage32(x, g, 1.0f, xg16, T, d_in, st);
-    if (e != cudaSuccess) return e;
-    const int BN = umma_pick_bn(T);
-    const int S = pick_splits(r, T, d_in, BN);
-    float* part = sc.take<float>((size_t)S * T * r);
-    DecSign dec{bits_vT, (int64_t)d_in / 32};
-    EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
-    e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, xg16, T, r, d_in, BN, S, st);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(finish_splitk_kernel, dim3((unsigned)((r + 31) / 32), (unsigned)((T + FIN_TC - 1) / FIN_TC)),
-                      dim3(32, 8), 0, st, (const float*)part, S, T, r, 1.0f, a_save, l, 1.0f,
-                      reinterpret_cast<uint16_t*>(al16), (const float*)nullptr, (float*)nullptr);
 }
 
 }  // namespace
@@ -354,22 +276,18 @@ tq2_status forward_one(const char* who, const uint32_t* bits_u, const uint32_t* 
                        const float* g, const float* x, float* y, float* a_save, float* c_save, int64_t T, int64_t d_in,
                        int64_t d_out, int64_t r, int accumulate, cudaStream_t st) {
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
-    const size_t bytes = (size_t)r * d_in / 8 + 256 + (size_t)T * d_in * 2 + 256 + (size_t)T * r * 2 + 256 +
-                         (size_t)8 * T * r * 4 + 256;
-    void* mem = nullptr;
-    cudaError_t e = cudaMallocAsync(&mem, bytes, st);
+    void* al16 = nullptr;
+    cudaError_t e = cudaMallocAsync(&al16, (size_t)T * r * 2, st);
     if (e != cudaSuccess) return cuda_status(e, who);
-    Scratch sc{reinterpret_cast<char*>(mem), 0};
-    uint32_t* bits_vT = sc.take<uint32_t>((size_t)r * d_in / 32);
-    void* al16 = sc.take<uint16_t>((size_t)T * r);
-    e = transpose_bits(bits_v, bits_vT, din, ir, st);
-    if (e == cudaSuccess) e = forward_a(bits_vT, x, g, l, a_save, al16, iT, din, ir, sc, st);
+    // a = (x.g) S_V (one pass over x), a_save, and f16(a.l) for the next GEMM
+    e = launch_blr_rank(x, g, 1.0f, bits_v, iT, din, ir, 1.0f, a_save, l, 1.0f, reinterpret_cast<uint16_t*>(al16),
+                        nullptr, nullptr, st);
     if (e == cudaSuccess) {
         DecSign dec{bits_u, (int64_t)r / 32};
         EpiArgs ep{y, c_save, h, nullptr, nullptr, (int64_t)d_out, 1.0f, accumulate};
-        e = launch_umma<DecSign, EPI_SCALE>(dec, ep, al16, iT, dout, ir, umma_pick_bn(iT), 1, st);
+        e = launch_umma<DecSign, EPI_SCALE>(dec, ep, al16, iT, dout, ir, blr_bn(iT), 1, st);
     }
-    cudaError_t e2 = cudaFreeAsync(mem, st);
+    cudaError_t e2 = cudaFreeAsync(al16, st);
     if (e != cudaSuccess) return cuda_status(e, who);
     return cuda_status(e2, who);
 }
@@ -381,52 +299,36 @@ tq2_status backward_one(const char* who, const uint32_t* bits_u, const uint32_t*
                         const float* c_save, float* dx, float* dh, float* dl, float* dg, int64_t T, int64_t d_in,
                         int64_t d_out, int64_t r, float gscale, int accumulate, cudaStream_t st) {
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
-    const int BN = umma_pick_bn(iT);
+    const int BN = blr_bn(iT);
     const int ttiles = (iT + BN - 1) / BN, chunks = (iT + FIN_TC - 1) / FIN_TC;
     const int64_t mx = d_in > d_out ? d_in : d_out;
-    const size_t bytes = (size_t)r * d_out / 8 + 256 + (size_t)T * mx * 2 + 256 + (size_t)T * r * 2 + 256 +
-                         (size_t)8 * T * r * 4 + 256 + (size_t)(ttiles + chunks + 2) * (mx + r) * 4 * 2 + 1024;
+    const size_t bytes = (size_t)T * r * 2 + 256 + (size_t)(ttiles > chunks ? ttiles : chunks) * (mx + r) * 4 + 1024;
     void* mem = nullptr;
     cudaError_t e = cudaMallocAsync(&mem, bytes, st);
     if (e != cudaSuccess) return cuda_status(e, who);
     Scratch sc{reinterpret_cast<char*>(mem), 0};
-    uint32_t* bits_uT = sc.take<uint32_t>((size_t)r * d_out / 32);
-    void* act16 = sc.take<uint16_t>((size_t)T * mx);        // dy.h.gs, then reused
-    void* r16 = sc.take<uint16_t>((size_t)T * r);           // a.l (dh recompute) / b.l.gs
+    uint16_t* r16 = sc.take<uint16_t>((size_t)T * r);         // a.l (dh recompute), then b.l.gs
     float* colp = sc.take<float>((size_t)(ttiles > chunks ? ttiles : chunks) * mx);
     const float inv_gs = 1.0f / gscale;
 
-    e = transpose_bits(bits_u, bits_uT, dout, ir, st);
     // dh += sum_t dy.c
-    if (e == cudaSuccess) {
-        if (c_save) {
-            e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
-                           dy, c_save, iT, dout, colp);
-            if (e == cudaSuccess) e = colsum_finish(colp, chunks, dout, dh, st);
-        } else {                                             // recompute c = (a.l) S_U^T in the GEMM
-            e = stage32(a_save, l, 1.0f, r16, iT, ir, st);
-            if (e == cudaSuccess) {
-                DecSign dec{bits_u, (int64_t)r / 32};
-                EpiArgs ep{nullptr, nullptr, nullptr, dy, colp, (int64_t)d_out, 1.0f};
-                e = launch_umma<DecSign, EPI_COLSUM>(dec, ep, r16, iT, dout, ir, BN, 1, st);
-            }
-            if (e == cudaSuccess) e = colsum_finish(colp, ttiles, dout, dh, st);
+    if (c_save) {
+        e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
+                       dy, c_save, iT, dout, colp);
+        if (e == cudaSuccess) e = colsum_finish(colp, chunks, dout, dh, st);
+    } else {                                                 // recompute c = (a.l) S_U^T in the GEMM
+        e = stage32(a_save, l, 1.0f, r16, iT, ir, st);
+        if (e == cudaSuccess) {
+            DecSign dec{bits_u, (int64_t)r / 32};
+            EpiArgs ep{nullptr, nullptr, nullptr, dy, colp, (int64_t)d_out, 1.0f};
+            e = launch_umma<DecSign, EPI_COLSUM>(dec, ep, r16, iT, dout, ir, BN, 1, st);
         }
+        if (e == cudaSuccess) e = colsum_finish(colp, ttiles, dout, dh, st);
     }
-    // b = (dy.h.gs) S_U / gs; dl += sum_t a.b; stage b.l.gs
-    if (e == cudaSuccess) e = stage32(dy, h, gscale, act16, iT, dout, st);
-    if (e == cudaSuccess) {
-        const int S = pick_splits(ir, iT, dout, BN);
-        float* part = sc.take<float>((size_t)S * T * r);
-        DecSign dec{bits_uT, (int64_t)d_out / 32};
-        EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
-        e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, act16, iT, ir, dout, BN, S, st);
-        if (e == cudaSuccess)
-            e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
-                           (const float*)part, S, iT, ir, inv_gs, (float*)nullptr, l, gscale,
-                           reinterpret_cast<uint16_t*>(r16), a_save, colp);
-        if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);
-    }
+    // b = (dy.h.gs) S_U / gs in one pass over dy; dl += sum_t a.b; stage f16(b.l.gs)
+    if (e == cudaSuccess)
+        e = launch_blr_rank(dy, h, gscale, bits_u, iT, dout, ir, inv_gs, nullptr, l, gscale, r16, a_save, colp, st);
+    if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);
     // dx' = (b.l.gs) S_V / gs; dx = g.dx'; dg += sum_t x.dx'
     if (e == cudaSuccess) {
         DecSign dec{bits_v, (int64_t)r / 32};
@@ -542,20 +444,15 @@ tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l
         return blr_fail(TQ2_EINVAL, "blr_sign_grads: x, dy, a_save, h, l and g must be 16-byte aligned");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
-    const int Tp = (iT + 63) / 64 * 64, BN = umma_pick_bn(iT), chunks = (iT + FIN_TC - 1) / FIN_TC;
-    const int S = pick_splits(ir, iT, dout, BN);
+    const int Tp = (iT + 63) / 64 * 64;
     const int64_t mx = d_in > d_out ? d_in : d_out;
-    const size_t bytes = (size_t)r * d_out / 8 + 256 + (size_t)T * d_out * 2 + 256 + (size_t)S * T * r * 4 + 256 +
-                         (size_t)T * r * 4 + 256 + (size_t)T * r * 2 + 256 + (size_t)(mx + r) * Tp * 2 + 512;
+    const size_t bytes = (size_t)T * r * 4 + 256 + (size_t)T * r * 2 + 256 + (size_t)(mx + r) * Tp * 2 + 512;
     void* mem = nullptr;
     cudaError_t e = cudaMallocAsync(&mem, bytes, st);
     if (e != cudaSuccess) return cuda_status(e, "blr_sign_grads: scratch");
     Scratch sc{reinterpret_cast<char*>(mem), 0};
-    uint32_t* bits_uT = sc.take<uint32_t>((size_t)r * d_out / 32);
-    void* act16 = sc.take<uint16_t>((size_t)T * d_out);
-    float* part = sc.take<float>((size_t)S * T * r);
     float* b32 = sc.take<float>((size_t)T * r);
-    uint16_t* b16 = sc.take<uint16_t>((size_t)T * r);      // the finish kernel's f16 staging (unused here)
+    uint16_t* b16 = sc.take<uint16_t>((size_t)T * r);      // the rank kernel's f16 staging (unused here)
     uint16_t* big = sc.take<uint16_t>((size_t)mx * Tp);     // (dy.h.gs)^T, then (x.g)^T
     uint16_t* small = sc.take<uint16_t>((size_t)r * Tp);    // (a.l)^T, then (b.l.gs)^T
     const float inv_gs = 1.0f / gscale;
@@ -582,17 +479,7 @@ tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l
         return launch_umma<DecDense, EPI_STORE>(dec, ep, rowsT, nrows, ir, Tp, bn, 1, st);
     };
     // b = (dy.h.gs) S_U / gs, as in the backward
-    e = transpose_bits(bits_u, bits_uT, dout, ir, st);
-    if (e == cudaSuccess) e = stage32(dy, h, gscale, act16, iT, dout, st);
-    if (e == cudaSuccess) {
-        DecSign dec{bits_uT, (int64_t)d_out / 32};
-        EpiArgs ep{part, nullptr, nullptr, nullptr, nullptr, (int64_t)r, 1.0f};
-        e = launch_umma<DecSign, EPI_PARTIAL>(dec, ep, act16, iT, ir, dout, BN, S, st);
-    }
-    if (e == cudaSuccess)
-        e = launch_pdl(finish_splitk_kernel, dim3((unsigned)((ir + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
-                       (const float*)part, S, iT, ir, inv_gs, b32, l, gscale, b16, (const float*)nullptr,
-                       (float*)nullptr);
+    e = launch_blr_rank(dy, h, gscale, bits_u, iT, dout, ir, inv_gs, b32, l, gscale, b16, nullptr, nullptr, st);
     // G_U = diag(h) dy^T a diag(l), from (dy.h.gs)^T and (a.l)^T
     if (e == cudaSuccess) e = stage_t(dy, dout, h, gscale, big);
     if (e == cudaSuccess) e = stage_t(a_save, ir, l, 1.0f, small);

@@ -1,0 +1,398 @@
+// blr_rank.cu -- the rank-space products of the binary low-rank layer
+// ("cortiq-engine 0.8.43, src/gpu_wgpu/train_mm.rs", blr_forward and
+// blr_backward):
+//
+//   forward   a[t,k] = sum_j (x[t,j] g[j]) S_V[j,k]               (K = d_in)
+//   backward  b[t,k] = sum_i (dy[t,i] h[i] gs) S_U[i,k] / gs       (K = d_out)
+//
+// as one pass over the f32 activations: the activation is read once from
+// HBM, scaled and rounded to f16 on chip, and multiplied by the sign plane on
+// the tensor cores; nothing but the [T][r] results goes back to memory.
+//
+// One CTA computes a 128-token x RB-rank tile (RB = 256, or 128 when r is
+// not a multiple of 256) over a slice of K; the CL CTAs of a cluster take
+// the CL slices of the same tile and add their partial sums through
+// distributed shared memory in a fixed order (deterministic).  Roles:
+//   * eight converter warps (two per 32-token lane quarter, alternate K
+//     stages) load their token's 64 activations of a stage, multiply by the
+//     column vector and the scale, round to f16 and store them into a ring in
+//     tensor memory: the MMA's A operand (tokens = M = 128 lanes);
+//   * four decoder warps expand the stage's 64 sign rows (the plane's row
+//     index is the GEMM's K) into the MMA's B operand in shared memory,
+//     MN-major (ranks contiguous) with 128-byte swizzling, so the bitmap is
+//     read in its own row order and never transposed; set bit -> +1.0,
+//     clear -> -1.0;
+//   * one warp issues tcgen05.mma (kind::f16, A from tensor memory, B from
+//     shared memory, f32 accumulation in tensor memory, N = RB);
+//   * the decoder warps then drain the accumulator into shared memory; after
+//     a cluster barrier CTA z sums rows [z*128/CL, (z+1)*128/CL) of the tile
+//     over the CL partials and writes the result, its f16 staging for the
+//     next GEMM, and (backward) the per-row-group partial column sums of
+//     result * other.
+// Within each 64-rank group the B operand holds ranks in the order the bits
+// fall out of a word: MN element 2p + h of the group is rank
+// (p < 16 ? 0 : 32) + p % 16 + 16 h.  That is also the order in which the
+// next GEMM (the core's DecSign decoder) expects its f16 operand inside every
+// 32-rank group, so the staged f16 row is the accumulator row as it stands.
+#include "tq2_internal.h"
+#include "umma_core.cuh"
+
+namespace tq2 {
+
+namespace {
+
+constexpr int BR_THREADS = 512;
+constexpr int BR_BK = 64;              // K per stage
+constexpr int BR_MAX_STAGES = 8;
+
+struct BrBars {
+    uint64_t full_a[BR_MAX_STAGES];
+    uint64_t full_b[BR_MAX_STAGES];
+    uint64_t empty[BR_MAX_STAGES];
+    uint64_t acc_full;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct BrArgs {
+    const float* act;          // [T][K] f32
+    const float* vec;          // [K] column factors of the activation
+    float scale;               // power of two multiplying the staged activation
+    const uint32_t* bits;      // [K][r/32], row j = plane row j (the GEMM's K index)
+    int T, K, r;
+    float oscale;              // result = accumulator * oscale
+    float* res;                // [T][r] f32 result, or null
+    const float* col;          // [r] factor of the f16 staging
+    float scale2;              // power of two of the f16 staging
+    uint16_t* st16;            // [T][r] f16 of result * col * scale2, 32-group pair order
+    const float* other;        // [T][r] or null: column sums of result * other
+    float* colpart;            // [T/32 chunks][r] partial column sums (rows of 32 tokens)
+};
+
+// rank offset inside a 64-rank group of MN element n (0..63)
+__device__ __forceinline__ int br_rank_of(int n) {
+    const int p = n >> 1, h = n & 1;
+    return (p < 16 ? 0 : 32) + (p & 15) + 16 * h;
+}
+
+}  // namespace
+
+template <int RB>
+__global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A, int S, int CL) {
+    constexpr int STAGE_B = BR_BK * RB * 2;                 // B stage bytes (64 K rows x RB ranks f16)
+    constexpr int NA = RB / 64;                             // MN atoms a stage
+    constexpr int RED_LD = RB + 4;                          // padded row of the drained partial (floats)
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int ring_bytes = S * STAGE_B > 128 * RED_LD * 4 ? S * STAGE_B : 128 * RED_LD * 4;
+    BrBars* bars = reinterpret_cast<BrBars*>(smem + ring_bytes + 16384);   // 16 KB guard after the ring
+    float* red = reinterpret_cast<float*>(smem);            // [128][RED_LD], after the mainloop
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int z = (int)cluster_ctarank();                   // K slice = rank in the cluster
+    const int rb = blockIdx.y, tile = blockIdx.z;
+    const int nk = A.K / BR_BK;
+    const int k0 = (int)(((int64_t)nk * z) / CL), k1 = (int)(((int64_t)nk * (z + 1)) / CL);
+    const int nst = k1 - k0;
+    const int wpr = A.r / 32;                               // words of a bitmap row
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bars->full_a[s], 4);
+            mbar_init(&bars->full_b[s], 4);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->acc_full, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512u);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t a_col0 = (uint32_t)RB;                   // A ring after the accumulator
+    volatile int* abort_flag = &bars->abort;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // ---- MMA issuer (whole warp; lane 0 waits, an elected lane issues)
+        const uint32_t idesc = idesc_f16_f32_bmn(128, (uint32_t)RB);
+        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+            int r = 1;
+            if (lane == 0) r = mbar_wait_or_abort(bar, parity, abort_flag, true) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, r, 0) != 0;
+        };
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int i = 0; i < nst; ++i) {
+            if (!wait1(&bars->full_a[s], ph) || !wait1(&bars->full_b[s], ph)) {
+                if (lane == 0) *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t bbase = smem_u32(smem + s * STAGE_B);
+            const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (BR_BK / 2));
+#pragma unroll
+            for (int j = 0; j < BR_BK / 16; ++j) {
+                // k16 step j = K atoms 2j, 2j+1 (each NA * 1024 bytes)
+                const uint64_t bdesc = sdesc_mnmajor_sw128(bbase + (uint32_t)(j * 2 * NA * 1024), 1024u,
+                                                           (uint32_t)(NA * 1024));
+                umma_f16_ts_elect(tmem, acol + (uint32_t)(j * 8), bdesc, idesc, (i > 0 || j > 0) ? 1u : 0u);
+            }
+            umma_commit_elect(&bars->empty[s]);
+            if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        if (ok) umma_commit_elect(&bars->acc_full);
+    } else if (warp >= 4 && warp < 12) {
+        // ---- converters: token row 32q + lane of the tile, stages of parity h
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        const int t = tile * 128 + q * 32 + lane;
+        const bool tok = t < A.T;
+        const float* arow = A.act + (int64_t)(tok ? t : 0) * A.K;
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a_col0;
+        pdl_wait();
+        for (int i = h; i < nst; i += 2) {
+            const int s = i % S;
+            const uint32_t ph = (uint32_t)(i / S) & 1u;
+            const int kb = (k0 + i) * BR_BK;
+            if (tok && i + 4 < nst) {                       // two stages of this warp ahead
+                prefetch_l2(arow + kb + 4 * BR_BK);
+                prefetch_l2(arow + kb + 4 * BR_BK + 32);
+            }
+            float4 v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                v[c] = tok ? __ldg(reinterpret_cast<const float4*>(arow + kb) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint32_t w[32];
+            const float4* vv = reinterpret_cast<const float4*>(A.vec + kb);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float4 g = __ldg(vv + c);
+                const __half2 lo = __floats2half2_rn(v[c].x * g.x * A.scale, v[c].y * g.y * A.scale);
+                const __half2 hi = __floats2half2_rn(v[c].z * g.z * A.scale, v[c].w * g.w * A.scale);
+                w[2 * c] = *reinterpret_cast<const uint32_t*>(&lo);
+                w[2 * c + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            tmem_st_32x32b_x32(taddr + (uint32_t)(s * (BR_BK / 2)), w);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->full_a[s]);
+        }
+    } else if (warp >= 12) {
+        // ---- decoders of the sign plane, then the accumulator drain
+        const int q = warp & 3, tid = q * 32 + lane;      // 0..127
+        pdl_wait();
+        constexpr int ITEMS = BR_BK * NA;                   // (row, 64-rank group) items a stage
+        for (int i = 0; i < nst; ++i) {
+            const int s = i % S;
+            const uint32_t ph = (uint32_t)(i / S) & 1u;
+            const int kb = (k0 + i) * BR_BK;
+            uint2 wv[ITEMS / 128];
+#pragma unroll
+            for (int u = 0; u < ITEMS / 128; ++u) {
+                const int it = tid + 128 * u, j = it / NA, na = it % NA;
+                wv[u] = __ldg(reinterpret_cast<const uint2*>(A.bits + (int64_t)(kb + j) * wpr + rb * (RB / 32) + 2 * na));
+            }
+            if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t* stage = smem + s * STAGE_B;
+#pragma unroll
+            for (int u = 0; u < ITEMS / 128; ++u) {
+                const int it = tid + 128 * u, j = it / NA, na = it % NA;
+                uint32_t c[32];
+                DecSign::word(wv[u].x, c);
+                DecSign::word(wv[u].y, c + 16);
+                // atom (K atom j/8, MN atom na), row j%8; chunk cc at cc ^ (j%8)
+                uint8_t* row = stage + (j >> 3) * (NA * 1024) + na * 1024 + (j & 7) * 128;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4*>(row + ((cc ^ (j & 7)) << 4)) =
+                        make_uint4(c[4 * cc], c[4 * cc + 1], c[4 * cc + 2], c[4 * cc + 3]);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->full_b[s]);
+        }
+        // drain: TMEM lane 32q + lane = token row of the tile
+        if (nst > 0 && mbar_wait_or_abort(&bars->acc_full, 0u, abort_flag)) {
+            tc_fence_after();
+            const uint32_t laddr = tmem + ((uint32_t)(q * 32) << 16);
+            float* rrow = red + (q * 32 + lane) * RED_LD;
+            for (int cc = 0; cc < RB; cc += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(laddr + (uint32_t)cc, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4)
+                    *reinterpret_cast<float4*>(rrow + cc + 4 * i4) =
+                        make_float4(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]),
+                                    __uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3]));
+            }
+        } else {
+            // no stage in this slice (or a wait gave up): a zero partial
+            for (int rr = 0; rr < 32; ++rr)
+                for (int i = lane; i < RB; i += 32) red[(q * 32 + rr) * RED_LD + i] = 0.f;
+        }
+    }
+
+    // every partial of the cluster is in shared memory
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+
+    // ---- reduction of rows [z*RPC, (z+1)*RPC) over the CL partials, in order.
+    // Warp w takes the 16 accumulator columns of segment w % NSEG and rows
+    // rgrp*32 + lane + p*32*ngrp of the CTA's share (rgrp = w / NSEG); each
+    // pass p covers one 32-token chunk, whose column sums of result * other
+    // are reduced over the lanes in a fixed butterfly order.
+    pdl_wait();                                             // col, other: earlier work on the stream
+    {
+        const int RPC = 128 / CL;                           // CL in {1, 2, 4}: a multiple of 32
+        constexpr int NSEG = RB / 16;
+        constexpr int NGRP = 16 / NSEG;
+        const int seg = warp % NSEG, rgrp = warp / NSEG;
+        const int n0 = seg * 16;                            // first accumulator column
+        // the segment's 16 columns: ranks kA..kA+7 (even columns) and kA+16..kA+23 (odd)
+        const int kA = rb * RB + (n0 >> 6) * 64 + br_rank_of(n0 & 63);
+        uint32_t base[4];
+        for (int zz = 0; zz < CL; ++zz) base[zz] = mapa_shared(smem_u32(red), (uint32_t)zz);
+        for (int p = 0; rgrp * 32 + p * 32 * NGRP < RPC; ++p) {
+            const int row = z * RPC + rgrp * 32 + p * 32 * NGRP + lane;
+            const int t = tile * 128 + row;
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int zz = 0; zz < CL; ++zz) {
+                const uint32_t a = base[zz] + (uint32_t)((row * RED_LD + n0) * 4);
+#pragma unroll
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    const float4 f = ld_dsmem_f4(a + 16u * i4);
+                    v[4 * i4] += f.x; v[4 * i4 + 1] += f.y; v[4 * i4 + 2] += f.z; v[4 * i4 + 3] += f.w;
+                }
+            }
+            const bool live = t < A.T;
+            const int64_t rowoff = (int64_t)(live ? t : 0) * A.r;
+            float cs[16];
+            __align__(16) uint16_t h16[16];
+            __align__(16) float r0[8], r1[8];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float val = v[i] * A.oscale;
+                const int k = kA + (i >> 1) + 16 * (i & 1);
+                if (i & 1) r1[i >> 1] = val; else r0[i >> 1] = val;
+                h16[i] = __half_as_ushort(__float2half_rn(val * A.col[k] * A.scale2));
+                cs[i] = (A.other && live) ? val * A.other[rowoff + k] : 0.f;
+            }
+            if (live) {
+                if (A.res) {
+                    float4* d0 = reinterpret_cast<float4*>(A.res + rowoff + kA);
+                    float4* d1 = reinterpret_cast<float4*>(A.res + rowoff + kA + 16);
+                    d0[0] = *reinterpret_cast<const float4*>(r0);
+                    d0[1] = *reinterpret_cast<const float4*>(r0 + 4);
+                    d1[0] = *reinterpret_cast<const float4*>(r1);
+                    d1[1] = *reinterpret_cast<const float4*>(r1 + 4);
+                }
+                // staged f16: the accumulator's column order is the 32-group pair order
+                uint4* dst = reinterpret_cast<uint4*>(A.st16 + rowoff + rb * RB + n0);
+                dst[0] = *reinterpret_cast<const uint4*>(h16);
+                dst[1] = *reinterpret_cast<const uint4*>(h16 + 8);
+            }
+            if (A.other) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float c = cs[i];
+                    c += __shfl_xor_sync(0xffffffffu, c, 16);
+                    c += __shfl_xor_sync(0xffffffffu, c, 8);
+                    c += __shfl_xor_sync(0xffffffffu, c, 4);
+                    c += __shfl_xor_sync(0xffffffffu, c, 2);
+                    c += __shfl_xor_sync(0xffffffffu, c, 1);
+                    cs[i] = c;
+                }
+                const int tc = t - lane;                    // first token of the chunk
+                if (lane < 16 && tc < A.T) {
+                    float mine = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i == lane) mine = cs[i];
+                    A.colpart[(int64_t)(tc / 32) * A.r + kA + (lane >> 1) + 16 * (lane & 1)] = mine;
+                }
+            }
+        }
+    }
+
+    // peers may still read this CTA's partial: leave together
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512u);
+    }
+}
+
+namespace {
+
+template <int RB>
+cudaError_t br_launch(const BrArgs& a, int T, cudaStream_t st) {
+    constexpr int STAGE_B = BR_BK * RB * 2;
+    const int S = RB == 256 ? 6 : 8;
+    const int red_bytes = 128 * (RB + 4) * 4;
+    const int ring = S * STAGE_B > red_bytes ? S * STAGE_B : red_bytes;
+    const size_t smem = (size_t)ring + 16384 + sizeof(BrBars) + 1024;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tiles = (T + 127) / 128, rbs = a.r / RB, nk = a.K / BR_BK;
+    // K slices a cluster: the largest of 4, 2, 1 that keeps every CTA of the
+    // grid resident at once and gives each slice at least two stages
+    int CL = 4;
+    while (CL > 1 && (CL * tiles * rbs > sms || nk < 2 * CL)) CL >>= 1;
+    cudaError_t e = cudaFuncSetAttribute(blr_rank_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)CL, (unsigned)rbs, (unsigned)tiles);
+    cfg.blockDim = dim3(BR_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, blr_rank_kernel<RB>, a, S, CL);
+}
+
+}  // namespace
+
+// res[t][k] = oscale * sum_j f16(act[t][j] * vec[j] * scale) * P[j][k] for the
+// sign plane P of `bits` ([K][r/32]); st16 = f16(res * col * scale2) in the
+// 32-group pair order; colpart[c][k] = sum over tokens 32c..32c+31 of
+// res * other (if other).  Requirements: K % 64 == 0, r % 128 == 0, act and
+// vec 16-byte aligned.
+cudaError_t launch_blr_rank(const float* act, const float* vec, float scale, const uint32_t* bits, int T, int K,
+                            int r, float oscale, float* res, const float* col, float scale2, uint16_t* st16,
+                            const float* other, float* colpart, cudaStream_t st) {
+    BrArgs a{act, vec, scale, bits, T, K, r, oscale, res, col, scale2, st16, other, colpart};
+    if (r % 256 == 0) return br_launch<256>(a, T, st);
+    return br_launch<128>(a, T, st);
+}
+
+}  // namespace tq2

@@ -69,6 +69,13 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
                           cudaStream_t st);
 unsigned int read_clear_dev_error_umma(cudaStream_t st);
 
+// blr_rank.cu: res = oscale * f16(act . vec * scale) P over the sign plane of
+// `bits` ([K][r/32], the plane's row index as the GEMM's K), f16 staging of
+// res * col * scale2 for the next GEMM, optional column sums of res * other.
+cudaError_t launch_blr_rank(const float* act, const float* vec, float scale, const uint32_t* bits, int T, int K,
+                            int r, float oscale, float* res, const float* col, float scale2, uint16_t* st16,
+                            const float* other, float* colpart, cudaStream_t st);
+
 // blr.cu
 cudaError_t launch_expand_bits(const uint32_t* bits, int64_t rows, int64_t r, uint16_t* plane, int transpose,
                                cudaStream_t st);

@@ -61,7 +61,13 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int splits = (tiles_n * tiles_m * 4 < sms * 3 && nk >= 4) ? 2 : 1;
+    // K splits: 1 or 2 (two partials add into a zeroed output in either
+    // order to the same sum); two only when they shorten the longest walk of
+    // a CTA (or CTA pair) over its units of work
+    const int cl = (BN > 128 && tiles_n >= 2) ? 2 : 1;
+    const int slots = sms / cl, units1 = ((tiles_n + cl - 1) / cl) * tiles_m;
+    auto longest = [&](int sp) { return ((units1 * sp + slots - 1) / slots) * ((nk + sp - 1) / sp); };
+    const int splits = (nk >= 4 && longest(2) < longest(1)) ? 2 : 1;
 
     uint32_t* xh = reinterpret_cast<uint32_t*>(scratch);
     const int64_t groups = (int64_t)M * (K / 16);

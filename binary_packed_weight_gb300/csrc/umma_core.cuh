@@ -125,7 +125,7 @@ struct DecSign {
     const uint32_t* bits;      // [rows][K/32]
     int64_t words;             // K/32
     static constexpr int PF = 3;
-    static constexpr bool PRIOR = false;
+    static constexpr bool PRIOR = true;    // the caller's bitmaps may come from the kernel before
     struct Raw { uint2 w; };
     __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
         Raw r;
@@ -180,7 +180,6 @@ struct DecDense {
 enum EpiMode : int {
     EPI_STORE = 0,        // out[t][n] = acc * oscale
     EPI_ATOMIC = 1,       // out[t][n] += acc * oscale (atomic; two K splits at most)
-    EPI_PARTIAL = 2,      // out[z][t][n] = acc (split-K partial, z = blockIdx.z)
     EPI_SCALE = 3,        // out[t][n] (+)= acc * oscale * vec[n]; out2[t][n] = acc * oscale if out2
     EPI_SCALE_COLSUM = 4, // as EPI_SCALE, plus colpart[tile][n] = sum_t acc*oscale*other[t][n]
     EPI_COLSUM = 5        // colpart[tile][n] = sum_t acc*oscale*other[t][n] only
@@ -217,15 +216,19 @@ struct TileMap {
     __device__ __forceinline__ int kc1(int z) const { return (int)(((int64_t)nk_total * (z + 1)) / splits); }
 };
 
-template <class Dec, int MODE>
+// AT: the decoded weights go to tensor memory (an S-stage ring of 32
+// columns a stage after the NACC accumulators) instead of shared memory, and
+// the MMAs read A from there; for token tiles of at most 128, where the
+// shared-memory round trip of the decoded rows would cost more than the MMAs.
+template <class Dec, int MODE, bool AT>
 __global__ void __launch_bounds__(UM_THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const EpiArgs ep, int T, int R, int BN,
                  int tmem_cols, const TileMap tm, int S, int NACC, int cl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_bytes = BN * 128;
-    uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned
-    UmmaBars* bars = reinterpret_cast<UmmaBars*>(a_ring + S * UM_A_STAGE);
+    uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned (!AT)
+    UmmaBars* bars = reinterpret_cast<UmmaBars*>(a_ring + (AT ? 0 : S * UM_A_STAGE));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
     // tiles of the same unit and share its activation tile: each loads 1/cl
@@ -257,6 +260,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     if (cl > 1) cluster_sync();                          // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    const uint32_t a_col0 = (uint32_t)(NACC * BN);       // first column of the A ring (AT)
     volatile int* abort_flag = &bars->abort;
 
     pdl_launch_dependents();
@@ -291,42 +295,57 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                 mbar_wait(&bars->full_b[i % S], (uint32_t)(i / S) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0) {                                   // ---- MMA issuer
-            const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
-            int lt = 0, s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units, ++lt) {
-                int np, m, z;
-                tm.decode(t, np, m, z);
-                const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
-                if (use >= 1 && !mbar_wait_or_abort(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u, abort_flag, true)) {
-                    *abort_flag = 1;
+        // ---- MMA issuer: the whole warp runs the loop, lane 0 waits on the
+        // barriers, and every MMA and commit is issued by one lane chosen with
+        // elect.sync, so the warp stays converged around the tcgen05 issue.
+        const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
+        int lt = 0, s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+            int r = 1;
+            if (lane == 0) r = mbar_wait_or_abort(bar, parity, abort_flag, true) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, r, 0) != 0;
+        };
+        for (int t = unit0; t < tm.total && ok; t += units, ++lt) {
+            int np, m, z;
+            tm.decode(t, np, m, z);
+            const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
+            if (use >= 1 && !wait1(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u)) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dcol = tmem + (uint32_t)(buf * BN);
+            const int k0 = tm.kc0(z), k1 = tm.kc1(z);
+            for (int kc = k0; kc < k1; ++kc) {
+                if (!wait1(&bars->full_b[s], ph) || !wait1(&bars->full_a[s], ph)) {
+                    if (lane == 0) *abort_flag = 1;
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dcol = tmem + (uint32_t)(buf * BN);
-                const int k0 = tm.kc0(z), k1 = tm.kc1(z);
-                for (int kc = k0; kc < k1; ++kc) {
-                    if (!mbar_wait_or_abort(&bars->full_b[s], ph, abort_flag, true) ||
-                        !mbar_wait_or_abort(&bars->full_a[s], ph, abort_flag, true)) {
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
+                const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
+                if (AT) {
+                    const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (UM_BK / 2));
+#pragma unroll
+                    for (int j = 0; j < UM_BK / 16; ++j)
+                        umma_f16_ts_elect(dcol, acol + (uint32_t)(j * 8), bdesc + (uint64_t)(2 * j), idesc,
+                                          (kc > k0 || j > 0) ? 1u : 0u);
+                } else {
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(a_ring + s * UM_A_STAGE));
 #pragma unroll
                     for (int j = 0; j < UM_BK / 16; ++j)
-                        umma_f16_ss(dcol, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j), idesc,
-                                    (kc > k0 || j > 0) ? 1u : 0u);
-                    if (cl > 1) umma_commit_mc(&bars->empty[s], cmask);
-                    else umma_commit(&bars->empty[s]);
-                    if (++s == S) { s = 0; ph ^= 1u; }
+                        umma_f16_ss_elect(dcol, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j), idesc,
+                                          (kc > k0 || j > 0) ? 1u : 0u);
                 }
-                umma_commit(&bars->acc_full[buf]);
+                if (cl > 1) umma_commit_mc_elect(&bars->empty[s], cmask);
+                else umma_commit_elect(&bars->empty[s]);
+                if (++s == S) { s = 0; ph ^= 1u; }
             }
+            if (!ok) break;
+            umma_commit_elect(&bars->acc_full[buf]);
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         }
     } else if (warp >= 4 && warp < 12) {                   // ---- decoders
         // warp pair (q, h): lane quarter q, stages with item parity h
@@ -389,14 +408,22 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                 }
                 uint32_t v[32];
                 dec.decode(cur, v);
-                // row arow of the stage: 16-byte chunk c (columns 4c..4c+3) at
-                // chunk c ^ (arow & 7), the layout TMA would write with 128-byte swizzle
-                uint8_t* rowp = a_ring + s * UM_A_STAGE + arow * 128;
+                if (AT) {
+                    // row arow = TMEM lane arow; pair j of the stage in column j of the stage's 32
+                    tc_fence_after();
+                    tmem_st_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)(s * (UM_BK / 2)), v);
+                    tmem_wait_st();
+                    tc_fence_before();
+                } else {
+                    // row arow of the stage: 16-byte chunk c (columns 4c..4c+3) at
+                    // chunk c ^ (arow & 7), the layout TMA would write with 128-byte swizzle
+                    uint8_t* rowp = a_ring + s * UM_A_STAGE + arow * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(rowp + ((c ^ (arow & 7)) << 4)) =
-                        make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                fence_proxy_async_shared();                // the MMA reads A through the async proxy
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(rowp + ((c ^ (arow & 7)) << 4)) =
+                            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                    fence_proxy_async_shared();            // the MMA reads A through the async proxy
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->full_a[s]);
             }
@@ -448,8 +475,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
                         ep.out[o] = a * ep.oscale;
                     } else if (MODE == EPI_ATOMIC) {
                         atomicAdd(ep.out + o, a * ep.oscale);
-                    } else if (MODE == EPI_PARTIAL) {
-                        ep.out[(int64_t)z * T * ep.ldo + o] = a;
                     } else {
                         const float w = a * ep.oscale;
                         if (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) {
@@ -486,28 +511,42 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
 }
 
 // Host: launch one GEMM.  act16 is f16 [T][K] (row pitch K), staged in the
-// decoder's K order; R = plane rows; splits = K splits.
+// decoder's K order; R = plane rows; splits = K splits.  Token tiles of at
+// most 128 keep the decoded weights in tensor memory (AT) and run without
+// clusters; wider tiles decode into shared memory and pair CTAs on
+// neighbouring weight tiles to share the activation tile.
 template <class Dec, int MODE>
 cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN, int splits,
-                        cudaStream_t st) {
-    if (BN > UM_MAX_BN || BN % 32 != 0 || BN < 32) return cudaErrorInvalidValue;
+                        cudaStream_t st);
+
+template <class Dec, int MODE, bool AT>
+cudaError_t launch_umma_impl(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
+                             int splits, cudaStream_t st) {
+    if (BN > UM_MAX_BN || BN % 16 != 0 || BN < 16 || (AT && BN > 128)) return cudaErrorInvalidValue;
+    // the epilogue drains 32 columns at a time: a tile narrower than a
+    // multiple of 32 must be the only token tile
+    if (BN % 32 != 0 && T > BN) return cudaErrorInvalidValue;
     const int tiles_n = (R + UM_BM - 1) / UM_BM;
-    const int cl = (tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
+    const int cl = (!AT && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
     CUtensorMap xmap;
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
                             (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // two accumulators in tensor memory (the epilogue of a tile overlaps the
-    // next tile's MMAs); the A and B stage rings fill the shared memory
+    // next tile's MMAs); the B ring (and the A ring unless AT) fills the
+    // shared memory; with AT the A ring takes S x 32 tensor-memory columns
+    // after the accumulators (2 x 128 + 8 x 32 = 512 at most)
     const int NACC = 2;
+    const int a_stage = AT ? 0 : UM_A_STAGE;
     int S = UM_STAGES;
-    while (S > 2 && (size_t)S * (BN * 128 + UM_A_STAGE) + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
+    while (S > 2 && (size_t)S * (BN * 128 + a_stage) + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
     int tmem_cols = 32;
-    while (tmem_cols < NACC * BN) tmem_cols <<= 1;
+    while (tmem_cols < NACC * BN + (AT ? S * (UM_BK / 2) : 0)) tmem_cols <<= 1;
+    if (tmem_cols > 512) return cudaErrorInvalidValue;
     // At least 120 KB of shared memory: no two CTAs of this kernel can share
     // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
     // (which a cluster barrier could otherwise turn into a deadlock).
-    size_t smem = (size_t)S * (BN * 128 + UM_A_STAGE) + 1024 + sizeof(UmmaBars) + 1024;
+    size_t smem = (size_t)S * (BN * 128 + a_stage) + 1024 + sizeof(UmmaBars) + 1024;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
     tm.tiles_n = tiles_n;
@@ -520,7 +559,7 @@ cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, in
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int units = tm.total < sms / cl ? tm.total : sms / cl;
-    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -537,12 +576,20 @@ cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, in
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE>, xmap, dec, ep, T, R, BN, tmem_cols, tm, S, NACC, cl);
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT>, xmap, dec, ep, T, R, BN, tmem_cols, tm, S, NACC,
+                              cl);
+}
+
+template <class Dec, int MODE>
+cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN, int splits,
+                        cudaStream_t st) {
+    if (BN <= 128) return launch_umma_impl<Dec, MODE, true>(dec, ep, act16, T, R, K, BN, splits, st);
+    return launch_umma_impl<Dec, MODE, false>(dec, ep, act16, T, R, K, BN, splits, st);
 }
 
 inline int umma_pick_bn(int T) {
     if (T >= 256) return 256;
-    return ((T + 31) / 32) * 32;
+    return ((T + 15) / 16) * 16;
 }
 
 }  // namespace tq2
