@@ -130,6 +130,7 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     if (!w) return fail(TQ2_ENOMEM, "tq2_upload: host allocation");
     w->N = N;
     w->K = K;
+    w->Np = (N + 127) / 128 * 128;
     cudaGetDevice(&w->device);
     // Both planes carry a little zeroed padding: the GEMV's TMA box may run up
     // to 128 bytes past the last row's codes, its scale copy up to 14 bytes.
@@ -137,8 +138,10 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     if (e == cudaSuccess) e = cudaMemset(w->codes + N * K / 4, 0, 128);
     if (e == cudaSuccess) e = cudaMalloc(&w->scales, (size_t)nblocks * 2 + 16);
     if (e == cudaSuccess) e = cudaMemset(w->scales + nblocks, 0, 16);
+    if (e == cudaSuccess) e = cudaMalloc(&w->scales_t, (size_t)(K / 128) * w->Np * 2);
     if (e != cudaSuccess) {
         cudaFree(w->codes);
+        cudaFree(w->scales);
         delete w;
         return cuda_fail(e, "tq2_upload: cudaMalloc");
     }
@@ -146,19 +149,22 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     e = cudaMallocAsync(reinterpret_cast<void**>(&tmp), aos_bytes, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(tmp, aos, aos_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = tq2::launch_repack(tmp, w->codes, w->scales, nblocks, st);
+    if (e == cudaSuccess) e = tq2::launch_scales_t(w->scales, w->scales_t, N, K / 128, w->Np, st);
     if (tmp) cudaFreeAsync(tmp, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         cudaFree(w->codes);
         cudaFree(w->scales);
+        cudaFree(w->scales_t);
         delete w;
         return cuda_fail(e, "tq2_upload");
     }
-    if (!tq2::make_gemv_maps(w)) {
+    if (!tq2::make_gemv_maps(w) || !tq2::make_umma_maps(w)) {
         cudaFree(w->codes);
         cudaFree(w->scales);
+        cudaFree(w->scales_t);
         delete w;
-        return fail(TQ2_EUNSUPPORTED, "tq2_upload: cuTensorMapEncodeTiled refused the code-plane map");
+        return fail(TQ2_EUNSUPPORTED, "tq2_upload: cuTensorMapEncodeTiled refused a code-plane map");
     }
     *out = w;
     return TQ2_OK;
@@ -168,7 +174,9 @@ tq2_status tq2_free(tq2_handle h) {
     if (!h) return TQ2_OK;
     cudaError_t e1 = cudaFree(h->codes);
     cudaError_t e2 = cudaFree(h->scales);
+    cudaError_t e3 = cudaFree(h->scales_t);
     delete h;
+    if (e3 != cudaSuccess) return cuda_fail(e3, "tq2_free");
     if (e1 != cudaSuccess) return cuda_fail(e1, "tq2_free");
     if (e2 != cudaSuccess) return cuda_fail(e2, "tq2_free");
     return TQ2_OK;

@@ -99,7 +99,7 @@ constexpr int FIN_TC = 32;
 
 // dst[c][t] = f16(src[t][c] * col[c] * scale) for t < T and 0 for T <= t < Tp:
 // an operand of a GEMM over the token axis, transposed so that the tokens
-// are its K (natural order, as DecDense and the TMA-loaded side expect).
+// are its K (natural order, as both TMA-loaded operands of the core expect).
 // 64 x 64 tiles through shared memory, 256 threads: 16-byte loads along c
 // (16 threads a token row), 4-byte stores of two tokens along t (32 threads,
 // 128 bytes, a c row).  C is a multiple of 64 (d_in, d_out, r).
@@ -283,9 +283,11 @@ tq2_status forward_one(const char* who, const uint32_t* bits_u, const uint32_t* 
     e = launch_blr_rank(x, g, 1.0f, bits_v, iT, din, ir, 1.0f, a_save, l, 1.0f, reinterpret_cast<uint16_t*>(al16),
                         nullptr, nullptr, st);
     if (e == cudaSuccess) {
-        DecSign dec{bits_u, (int64_t)r / 32};
+        PlaneMaps pm;
         EpiArgs ep{y, c_save, h, nullptr, nullptr, (int64_t)d_out, 1.0f, accumulate};
-        e = launch_umma<DecSign, EPI_SCALE>(dec, ep, al16, iT, dout, ir, blr_bn(iT), 1, st);
+        e = plane_maps_sign(pm, bits_u, dout, ir) ? launch_umma<DecSign, EPI_SCALE>(pm, ep, al16, iT, dout, ir,
+                                                                                    blr_bn(iT), 1, st)
+                                                  : cudaErrorInvalidValue;
     }
     cudaError_t e2 = cudaFreeAsync(al16, st);
     if (e != cudaSuccess) return cuda_status(e, who);
@@ -319,9 +321,11 @@ tq2_status backward_one(const char* who, const uint32_t* bits_u, const uint32_t*
     } else {                                                 // recompute c = (a.l) S_U^T in the GEMM
         e = stage32(a_save, l, 1.0f, r16, iT, ir, st);
         if (e == cudaSuccess) {
-            DecSign dec{bits_u, (int64_t)r / 32};
+            PlaneMaps pm;
             EpiArgs ep{nullptr, nullptr, nullptr, dy, colp, (int64_t)d_out, 1.0f};
-            e = launch_umma<DecSign, EPI_COLSUM>(dec, ep, r16, iT, dout, ir, BN, 1, st);
+            e = plane_maps_sign(pm, bits_u, dout, ir)
+                    ? launch_umma<DecSign, EPI_COLSUM>(pm, ep, r16, iT, dout, ir, BN, 1, st)
+                    : cudaErrorInvalidValue;
         }
         if (e == cudaSuccess) e = colsum_finish(colp, ttiles, dout, dh, st);
     }
@@ -331,9 +335,11 @@ tq2_status backward_one(const char* who, const uint32_t* bits_u, const uint32_t*
     if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);
     // dx' = (b.l.gs) S_V / gs; dx = g.dx'; dg += sum_t x.dx'
     if (e == cudaSuccess) {
-        DecSign dec{bits_v, (int64_t)r / 32};
+        PlaneMaps pm;
         EpiArgs ep{dx, nullptr, g, x, colp, (int64_t)d_in, inv_gs, accumulate};
-        e = launch_umma<DecSign, EPI_SCALE_COLSUM>(dec, ep, r16, iT, din, ir, BN, 1, st);
+        e = plane_maps_sign(pm, bits_v, din, ir)
+                ? launch_umma<DecSign, EPI_SCALE_COLSUM>(pm, ep, r16, iT, din, ir, BN, 1, st)
+                : cudaErrorInvalidValue;
         if (e == cudaSuccess) e = colsum_finish(colp, ttiles, din, dg, st);
     }
     cudaError_t e2 = cudaFreeAsync(mem, st);
@@ -469,14 +475,15 @@ tq2_status blr_sign_grads(const uint32_t* bits_u, const float* h, const float* l
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         const int bn = umma_pick_bn(nrows);
         const int tiles = ((ir + UM_BM - 1) / UM_BM) * ((nrows + bn - 1) / bn);
-        DecDense dec{colsT, (int64_t)Tp};
+        PlaneMaps pm;
+        if (!plane_maps_dense(pm, colsT, ir, Tp)) return cudaErrorInvalidValue;
         EpiArgs ep{G, nullptr, nullptr, nullptr, nullptr, (int64_t)r, inv_gs};
         if (tiles < sms && Tp >= 2 * UM_BK) {
             cudaError_t e1 = cudaMemsetAsync(G, 0, (size_t)nrows * r * sizeof(float), st);
             if (e1 != cudaSuccess) return e1;
-            return launch_umma<DecDense, EPI_ATOMIC>(dec, ep, rowsT, nrows, ir, Tp, bn, 2, st);
+            return launch_umma<DecDense, EPI_ATOMIC>(pm, ep, rowsT, nrows, ir, Tp, bn, 2, st);
         }
-        return launch_umma<DecDense, EPI_STORE>(dec, ep, rowsT, nrows, ir, Tp, bn, 1, st);
+        return launch_umma<DecDense, EPI_STORE>(pm, ep, rowsT, nrows, ir, Tp, bn, 1, st);
     };
     // b = (dy.h.gs) S_U / gs, as in the backward
     e = launch_blr_rank(dy, h, gscale, bits_u, iT, dout, ir, inv_gs, b32, l, gscale, b16, nullptr, nullptr, st);

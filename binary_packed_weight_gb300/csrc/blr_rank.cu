@@ -13,10 +13,13 @@
 // not a multiple of 256) over a slice of K; the CL CTAs of a cluster take
 // the CL slices of the same tile and add their partial sums through
 // distributed shared memory in a fixed order (deterministic).  Roles:
-//   * eight converter warps (two per 32-token lane quarter, alternate K
-//     stages) load their token's 64 activations of a stage, multiply by the
-//     column vector and the scale, round to f16 and store them into a ring in
-//     tensor memory: the MMA's A operand (tokens = M = 128 lanes);
+//   * one thread streams the f32 activation tile of each stage (128 tokens x
+//     64) into shared memory with TMA (two 32-column boxes, 128-byte swizzle);
+//   * eight converter warps (two per 32-token lane quarter, one per 32-column
+//     half of a stage) read their token's activations of every stage from
+//     there, multiply by the column vector and the scale, round to f16 and
+//     store them into a ring in tensor memory: the MMA's A operand (tokens =
+//     M = 128 lanes);
 //   * four decoder warps expand the stage's 64 sign rows (the plane's row
 //     index is the GEMM's K) into the MMA's B operand in shared memory,
 //     MN-major (ranks contiguous) with 128-byte swizzling, so the bitmap is
@@ -46,6 +49,8 @@ constexpr int BR_BK = 64;              // K per stage
 constexpr int BR_MAX_STAGES = 8;
 
 struct BrBars {
+    uint64_t xfull[BR_MAX_STAGES];
+    uint64_t xempty[BR_MAX_STAGES];
     uint64_t full_a[BR_MAX_STAGES];
     uint64_t full_b[BR_MAX_STAGES];
     uint64_t empty[BR_MAX_STAGES];
@@ -78,14 +83,18 @@ __device__ __forceinline__ int br_rank_of(int n) {
 }  // namespace
 
 template <int RB>
-__global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A, int S, int CL) {
+__global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                 const BrArgs A, int S, int CL) {
     constexpr int STAGE_B = BR_BK * RB * 2;                 // B stage bytes (64 K rows x RB ranks f16)
+    constexpr int STAGE_X = BR_BK * 128 * 4;                // activation stage bytes (128 tokens x 64 f32)
     constexpr int NA = RB / 64;                             // MN atoms a stage
     constexpr int RED_LD = RB + 4;                          // padded row of the drained partial (floats)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int ring_bytes = S * STAGE_B > 128 * RED_LD * 4 ? S * STAGE_B : 128 * RED_LD * 4;
-    BrBars* bars = reinterpret_cast<BrBars*>(smem + ring_bytes + 16384);   // 16 KB guard after the ring
+    uint8_t* bring = smem;                                  // [S][STAGE_B] sign-plane operand
+    uint8_t* xring = smem + S * STAGE_B;                    // [S][STAGE_X] activation tiles
+    const int ring_bytes = S * (STAGE_B + STAGE_X) > 128 * RED_LD * 4 ? S * (STAGE_B + STAGE_X) : 128 * RED_LD * 4;
+    BrBars* bars = reinterpret_cast<BrBars*>(smem + ring_bytes + 16384);   // 16 KB guard after the rings
     float* red = reinterpret_cast<float*>(smem);            // [128][RED_LD], after the mainloop
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -98,13 +107,16 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&bars->full_a[s], 4);
+            mbar_init(&bars->xfull[s], 1);
+            mbar_init(&bars->xempty[s], 8);
+            mbar_init(&bars->full_a[s], 8);
             mbar_init(&bars->full_b[s], 4);
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->acc_full, 1);
         bars->abort = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&xmap);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, 512u);
@@ -136,7 +148,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A,
                 break;
             }
             tc_fence_after();
-            const uint32_t bbase = smem_u32(smem + s * STAGE_B);
+            const uint32_t bbase = smem_u32(bring + s * STAGE_B);
             const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (BR_BK / 2));
 #pragma unroll
             for (int j = 0; j < BR_BK / 16; ++j) {
@@ -149,42 +161,65 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A,
             if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (ok) umma_commit_elect(&bars->acc_full);
+    } else if (warp == 2) {
+        // ---- TMA producer of the activation tiles
+        if (lane == 0) {
+            pdl_wait();
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (uint32_t)(i / S) & 1u;
+                if (i >= S && !mbar_wait_or_abort(&bars->xempty[s], ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->xfull[s], (uint32_t)STAGE_X);
+                const int kx = (k0 + i) * BR_BK;
+                tma_load_2d(xring + s * STAGE_X, &xmap, &bars->xfull[s], kx, tile * 128);
+                tma_load_2d(xring + s * STAGE_X + STAGE_X / 2, &xmap, &bars->xfull[s], kx + 32, tile * 128);
+            }
+        }
     } else if (warp >= 4 && warp < 12) {
-        // ---- converters: token row 32q + lane of the tile, stages of parity h
+        // ---- converters: token row 32q + lane of the tile, columns 32h..32h+31
+        // of every stage (box h of the stage's activation tile).  Every
+        // converter warp takes every stage, so no warp can run a ring round
+        // ahead of another: a wait on a phase parity is never ambiguous.
         const int q = warp & 3, h = (warp - 4) >> 2;
-        const int t = tile * 128 + q * 32 + lane;
-        const bool tok = t < A.T;
-        const float* arow = A.act + (int64_t)(tok ? t : 0) * A.K;
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a_col0;
-        pdl_wait();
-        for (int i = h; i < nst; i += 2) {
+        const int i_row = q * 32 + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)(16 * h);
+        pdl_wait();                                         // the column vector may come from earlier work
+        for (int i = 0; i < nst; ++i) {
             const int s = i % S;
             const uint32_t ph = (uint32_t)(i / S) & 1u;
-            const int kb = (k0 + i) * BR_BK;
-            if (tok && i + 4 < nst) {                       // two stages of this warp ahead
-                prefetch_l2(arow + kb + 4 * BR_BK);
-                prefetch_l2(arow + kb + 4 * BR_BK + 32);
+            const int kb = (k0 + i) * BR_BK + 32 * h;
+            if (!mbar_wait_or_abort(&bars->xfull[s], ph, abort_flag)) {
+                *abort_flag = 1;
+                break;
             }
-            float4 v[16];
+            // row i_row of box h: 16-byte chunk c (columns 32h + 4c..) at chunk c ^ (i_row & 7)
+            // The slot goes back to the TMA producer only after the values read
+            // from it have been used, and after a proxy fence: the next write
+            // into it comes through the async proxy.
+            uint32_t w[16];
+            const uint8_t* xr = xring + s * STAGE_X + h * (STAGE_X / 2) + i_row * 128;
+            const float4* vv = reinterpret_cast<const float4*>(A.vec + kb);
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                v[c] = tok ? __ldg(reinterpret_cast<const float4*>(arow + kb) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(xr + ((c ^ (i_row & 7)) << 4));
+                const float4 g = __ldg(vv + c);
+                const __half2 lo = __floats2half2_rn(v.x * g.x * A.scale, v.y * g.y * A.scale);
+                const __half2 hi = __floats2half2_rn(v.z * g.z * A.scale, v.w * g.w * A.scale);
+                w[2 * c] = *reinterpret_cast<const uint32_t*>(&lo);
+                w[2 * c + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xempty[s]);
             if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            uint32_t w[32];
-            const float4* vv = reinterpret_cast<const float4*>(A.vec + kb);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 g = __ldg(vv + c);
-                const __half2 lo = __floats2half2_rn(v[c].x * g.x * A.scale, v[c].y * g.y * A.scale);
-                const __half2 hi = __floats2half2_rn(v[c].z * g.z * A.scale, v[c].w * g.w * A.scale);
-                w[2 * c] = *reinterpret_cast<const uint32_t*>(&lo);
-                w[2 * c + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-            }
-            tmem_st_32x32b_x32(taddr + (uint32_t)(s * (BR_BK / 2)), w);
+            tmem_st_32x32b_x16(taddr + (uint32_t)(s * (BR_BK / 2)), w);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -209,7 +244,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const BrArgs A,
                 *abort_flag = 1;
                 break;
             }
-            uint8_t* stage = smem + s * STAGE_B;
+            uint8_t* stage = bring + s * STAGE_B;
 #pragma unroll
             for (int u = 0; u < ITEMS / 128; ++u) {
                 const int it = tid + 128 * u, j = it / NA, na = it % NA;
@@ -349,9 +384,15 @@ namespace {
 template <int RB>
 cudaError_t br_launch(const BrArgs& a, int T, cudaStream_t st) {
     constexpr int STAGE_B = BR_BK * RB * 2;
-    const int S = RB == 256 ? 6 : 8;
+    constexpr int STAGE_X = BR_BK * 128 * 4;
+    const int S = RB == 256 ? 3 : 4;
     const int red_bytes = 128 * (RB + 4) * 4;
-    const int ring = S * STAGE_B > red_bytes ? S * STAGE_B : red_bytes;
+    const int ring = S * (STAGE_B + STAGE_X) > red_bytes ? S * (STAGE_B + STAGE_X) : red_bytes;
+    // the activation [T][K] f32 as 32-column x 128-token boxes, 128-byte swizzle
+    CUtensorMap xmap;
+    if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(a.act), (uint64_t)a.K,
+                            (uint64_t)T, (uint64_t)a.K * 4, 32u, 128u, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     const size_t smem = (size_t)ring + 16384 + sizeof(BrBars) + 1024;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -377,7 +418,7 @@ cudaError_t br_launch(const BrArgs& a, int T, cudaStream_t st) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, blr_rank_kernel<RB>, a, S, CL);
+    return cudaLaunchKernelEx(&cfg, blr_rank_kernel<RB>, xmap, a, S, CL);
 }
 
 }  // namespace

@@ -7,15 +7,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+namespace tq2 {
+// Tensor maps of a plane for the tcgen05 core (umma_core.cuh).
+struct PlaneMaps {
+    CUtensorMap m0, m1;
+};
+}  // namespace tq2
+
 struct tq2_weight {
     int64_t N = 0, K = 0;
+    int64_t Np = 0;                // N rounded up to a multiple of 128
     uint8_t* codes = nullptr;      // [N][K/4], then 128 bytes of padding
     uint16_t* scales = nullptr;    // [N][K/128] f16 bits, then 16 bytes of padding
+    uint16_t* scales_t = nullptr;  // [K/128][Np] the same bits block-major (rows >= N zero), for the tensor path
     int device = 0;
     // 3D views of the code plane for the GEMV's TMA loads, built at upload:
     // (128-byte piece, row, piece index), strides (1, K/4, 128) bytes; boxes
     // of 16 rows x 8 pieces (k-split units) and 128 rows x 1 piece (row units).
     CUtensorMap gemv_map_k, gemv_map_r;
+    // the tensor path's views: code tiles of 128 rows x 16 bytes and
+    // block-major scale rows of 128 (umma_core.cuh, plane_maps_tq2)
+    tq2::PlaneMaps umma_maps;
 };
 
 namespace tq2 {
@@ -44,6 +56,8 @@ cudaError_t launch_repack(const uint8_t* aos_dev, uint8_t* codes, uint16_t* scal
                           cudaStream_t st);
 cudaError_t launch_unpack(const uint8_t* codes, const uint16_t* scales, uint8_t* aos_dev, int64_t nblocks,
                           cudaStream_t st);
+cudaError_t launch_scales_t(const uint16_t* scales, uint16_t* scales_t, int64_t N, int64_t nb, int64_t Np,
+                            cudaStream_t st);
 cudaError_t launch_dequant_f16(const uint8_t* codes, const uint16_t* scales, uint16_t* w, int64_t N,
                                int64_t K, cudaStream_t st);
 size_t skinny_scratch_bytes(int64_t M, int64_t K);
@@ -64,6 +78,7 @@ cudaError_t launch_gemv(const tq2_weight* const* ws, const float* const* xs, flo
 unsigned int read_clear_dev_error_gemv(cudaStream_t st);
 
 // tq2_umma.cu
+bool make_umma_maps(tq2_weight* w);
 size_t tensor_scratch_bytes(int64_t M, int64_t K);
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
                           cudaStream_t st);

@@ -53,6 +53,16 @@ __global__ void unpack_soa_kernel(const uint8_t* __restrict__ codes, const uint1
     }
 }
 
+// Block-major copy of the scale plane for the tensor path: scales_t[b][n] =
+// scales[n][b] for n < N, 0 for N <= n < Np.
+__global__ void scales_t_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ scales_t, int64_t N,
+                                int64_t nb, int64_t Np) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= nb * Np) return;
+    const int64_t b = i / Np, n = i % Np;
+    scales_t[i] = n < N ? scales[n * nb + b] : (uint16_t)0;
+}
+
 // W as f16 bits, natural order, through the same pair decode the GEMMs use:
 // one thread per 32-bit code word (16 elements).
 __global__ void dequant_f16_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
@@ -242,6 +252,13 @@ cudaError_t launch_repack(const uint8_t* aos_dev, uint8_t* codes, uint16_t* scal
                           cudaStream_t st) {
     const int64_t n = nblocks * 32;
     repack_aos_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(aos_dev, codes, scales, nblocks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scales_t(const uint16_t* scales, uint16_t* scales_t, int64_t N, int64_t nb, int64_t Np,
+                            cudaStream_t st) {
+    const int64_t n = nb * Np;
+    scales_t_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(scales, scales_t, N, nb, Np);
     return cudaGetLastError();
 }
 

@@ -8,11 +8,13 @@
 // that page relies on the same fact), so the block scale needs no epilogue.
 //
 // The GEMM runs on the persistent tcgen05 core (umma_core.cuh) with the TQ2
-// decoder: a CTA computes 128 weight rows x BN tokens of out^T; decoder warps
-// write the f16 weight rows into a shared-memory ring in the MMA's swizzled
-// layout, TMA brings the f16 activation tiles, one thread issues the MMAs
-// into two tensor-memory accumulators, and four epilogue warps store
-// out[m][n] while the next tile's MMAs run.
+// decoder: a CTA computes 128 weight rows x BN tokens of out^T; TMA streams
+// the 2-bit code tiles and block scales into a deep shared-memory ring and
+// the f16 activation tiles into another; decoder warps expand the codes into
+// the f16 A operand (tensor memory for BN <= 128, else a swizzled
+// shared-memory ring); one warp issues the MMAs into two tensor-memory
+// accumulators, and four epilogue warps store out[m][n] while the next
+// tile's MMAs run.
 // The K order inside every 16-element group is permuted the same way on both
 // operands: position 2q holds element q and 2q+1 holds element q+8, which is
 // the order in which two-code pairs fall out of a 32-bit code word.
@@ -51,6 +53,10 @@ __global__ void stage_x_f16_kernel(const float* __restrict__ x, uint32_t* __rest
 
 size_t tensor_scratch_bytes(int64_t M, int64_t K) { return (size_t)(M * K * 2); }
 
+bool make_umma_maps(tq2_weight* w) {
+    return plane_maps_tq2(w->umma_maps, w->codes, w->scales_t, (int)w->N, (int)w->K, (int)w->Np);
+}
+
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
                           cudaStream_t st) {
     const int N = (int)w->N, K = (int)w->K;
@@ -78,10 +84,9 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
                                (int64_t)K, out, splits > 1 ? (int64_t)M * N : (int64_t)0);
     if (e != cudaSuccess) return e;
 
-    DecTQ2 dec{w->codes, w->scales, (int64_t)K / 4, K / 128};
     EpiArgs ep{out, nullptr, nullptr, nullptr, nullptr, (int64_t)N, 1.0f};
-    if (splits > 1) return launch_umma<DecTQ2, EPI_ATOMIC>(dec, ep, xh, M, N, K, BN, splits, st);
-    return launch_umma<DecTQ2, EPI_STORE>(dec, ep, xh, M, N, K, BN, 1, st);
+    if (splits > 1) return launch_umma<DecTQ2, EPI_ATOMIC>(w->umma_maps, ep, xh, M, N, K, BN, splits, st);
+    return launch_umma<DecTQ2, EPI_STORE>(w->umma_maps, ep, xh, M, N, K, BN, 1, st);
 }
 
 unsigned int read_clear_dev_error_umma(cudaStream_t st) {

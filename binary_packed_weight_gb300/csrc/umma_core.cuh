@@ -3,18 +3,24 @@
 //
 //   D[t, n] = sum_k act[t, k] * P[n, k]
 //
-// P is a packed plane (2-bit ternary codes with f16 block scales, or 1-bit
-// signs) decoded on chip; act is an f16 activation matrix staged in the K
+// P is a packed plane (2-bit ternary codes with f16 block scales, 1-bit
+// signs) or dense f16 rows; act is an f16 activation matrix staged in the K
 // order the decoder emits pairs in.  One CTA computes a 128 (plane rows) x BN
 // (tokens) tile:
-//   * eight decoder warps (one plane row per thread, two warps per row
-//     quarter taking alternate K stages) write the decoded f16 rows into a
-//     shared-memory ring in the MMA's K-major 128-byte-swizzled layout, so
-//     tensor memory holds only the two accumulators;
-//   * one thread issues TMA loads of the activation tile (B operand, 128-byte
-//     swizzle) into a 4-stage shared-memory ring;
-//   * one thread issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
-//     one of two accumulators and frees stages with tcgen05.commit;
+//   * one thread streams the activation tiles (B operand, 128-byte swizzle)
+//     into a ring of up to 8 stages with TMA;
+//   * a second thread streams the packed plane tiles of the same stages (the
+//     2-bit codes and block scales, or the sign words) with TMA into a
+//     deeper ring of raw stages, far enough ahead to cover the HBM latency;
+//     dense f16 rows skip the decoders: TMA writes them as the A operand;
+//   * eight decoder warps (one plane row per thread, two warps per 32-row
+//     quarter taking alternate stages) expand a raw stage from shared memory
+//     into the f16 A operand: into tensor memory when the token tile is at
+//     most 128 wide (AT), otherwise into a shared-memory ring in the MMA's
+//     K-major 128-byte-swizzled layout;
+//   * one warp issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
+//     one of two accumulators and frees stages with tcgen05.commit; every
+//     MMA is issued by one lane of the converged warp (elect.sync);
 //   * four epilogue warps read the finished accumulator (tcgen05.ld), hand it
 //     back, and run the epilogue policy of the call while the next tile's
 //     MMAs proceed in the other accumulator.
@@ -28,10 +34,11 @@ namespace tq2 {
 
 constexpr int UM_BM = 128;       // plane rows per tile = MMA M
 constexpr int UM_BK = 64;        // K per pipeline stage (128 bytes of f16)
-constexpr int UM_STAGES = 8;     // ring slots allocated; the launch picks how many it uses
+constexpr int UM_STAGES = 8;     // B / A ring slots allocated; the launch picks how many it uses
+constexpr int UM_RAW_STAGES = 32;   // raw plane ring slots allocated
 constexpr int UM_MAX_BN = 256;   // MMA N limit for M = 128
 constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in shared memory (16 KB)
-// warp 0 TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 idle,
+// warp 0 activation TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 plane TMA,
 // warps 4-11 decoders (two per 32-row quarter of the tile, taking alternate stages),
 // warps 12-15 epilogue (one per lane quarter)
 constexpr int UM_THREADS = 512;
@@ -40,71 +47,41 @@ struct UmmaBars {
     uint64_t full_b[UM_STAGES];
     uint64_t full_a[UM_STAGES];
     uint64_t empty[UM_STAGES];
+    uint64_t raw_full[UM_RAW_STAGES];
+    uint64_t raw_empty[UM_RAW_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-__device__ __forceinline__ uint4 ldg_u4_nc(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ldg_u2_nc(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
 // ---------------------------------------------------------------- decoders ----
-// A decoder turns K-stage kc (64 elements) of plane row `row` (valid iff ok)
-// into 32 f16 pairs v[0..31]: pair j of the row holds K positions 2j, 2j+1 of
-// the permuted order the activations are staged in (16-byte chunk j/4 of the
-// row's 128 bytes, before the swizzle).  Loads go
-// through L1 (the neighbouring stage of the same 32-byte sector is read by
-// the partner decoder warp).
+// A decoder describes the plane: RAW bytes a stage of its packed tile (TMA
+// loads issued by issue()), and decode(), which turns row r (0..127) of a
+// raw stage of K-stage kc (64 elements) into 32 f16 pairs v[0..31]: pair j
+// holds K positions 2j, 2j+1 of the permuted order the activations are staged
+// in (16-byte chunk j/4 of the row's 128 bytes, before the swizzle).
+// DIRECT planes are already f16 in that order: TMA writes them as the A
+// operand and no decoder runs.
 
-__device__ __forceinline__ uint4 ldg_u4_l1(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ldg_u2_l1(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
-// TQ2 codes: 16 bytes (four 16-element words) per stage, element e of a word
-// at bits 2e; pair q = (element q, element q+8); the block scale is folded
-// in: (c-1)*d is exact in f16.  Activations staged in 16-element groups.
+// TQ2 codes: 16 bytes (four 16-element words) per row and stage, element e
+// of a word at bits 2e; pair q = (element q, element q+8); the block scale is
+// folded in: (c-1)*d is exact in f16.  Activations staged in 16-element
+// groups.  Raw stage: codes [128 rows][16 B], then the stage's block scales
+// [128 rows] (from the block-major copy of the scale plane made at upload).
 struct DecTQ2 {
-    const uint8_t* codes;      // [rows][K/4]
-    const uint16_t* scales;    // [rows][K/128]
-    int64_t pitch;             // K/4
-    int nb;                    // K/128
-    static constexpr int PF = 3;   // stages each decoder warp loads ahead
-    static constexpr bool PRIOR = false;   // rows written by earlier work on the stream (wait for it)
-    struct Raw { uint4 c; uint16_t d; };
-    __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
-        Raw r;
-        if (ok) {
-            r.c = ldg_u4_l1(codes + (int64_t)row * pitch + (int64_t)kc * 16);
-            r.d = __ldg(scales + (int64_t)row * nb + kc / 2);
-        } else {
-            r.c = make_uint4(0u, 0u, 0u, 0u);
-            r.d = 0;
-        }
-        return r;
+    static constexpr int RAW = UM_BM * 16 + UM_BM * 2;
+    static constexpr bool DIRECT = false;
+    __device__ __forceinline__ static void issue(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* raw,
+                                                 uint64_t* bar, int row0, int kc) {
+        tma_load_2d(raw, m0, bar, kc * 16, row0);              // codes: x in bytes
+        tma_load_2d(raw + UM_BM * 16, m1, bar, row0, kc / 2);   // scales: x = row, y = block
     }
-    __device__ __forceinline__ void decode(const Raw& r, uint32_t (&v)[32]) const {
-        const __half2 d2 = __halves2half2(__ushort_as_half(r.d), __ushort_as_half(r.d));
-        const uint32_t words[4] = {r.c.x, r.c.y, r.c.z, r.c.w};
+    __device__ __forceinline__ static void decode(const uint8_t* raw, int r, int kc, uint32_t (&v)[32]) {
+        const uint4 c = *reinterpret_cast<const uint4*>(raw + r * 16);
+        const uint16_t d = reinterpret_cast<const uint16_t*>(raw + UM_BM * 16)[r];
+        const __half2 d2 = __halves2half2(__ushort_as_half(d), __ushort_as_half(d));
+        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
         uint32_t p[8];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -115,23 +92,17 @@ struct DecTQ2 {
                 v[w * 8 + q] = *reinterpret_cast<uint32_t*>(&hh);
             }
         }
+        (void)kc;
     }
 };
 
-// Sign bits: two 32-sign words per stage (bit b = element b of a word, set =
-// +1); pair p = (element p, element p+16).  Activations staged in 32-element
-// groups.
+// Sign bits: two 32-sign words per row and stage (bit b = element b of a
+// word, set = +1); pair p = (element p, element p+16).  Activations staged in
+// 32-element groups.  Raw stage: [128 rows][4 words], the words of stages
+// kc & ~1 and kc | 1 (a TMA box is at least 16 bytes wide).
 struct DecSign {
-    const uint32_t* bits;      // [rows][K/32]
-    int64_t words;             // K/32
-    static constexpr int PF = 3;
-    static constexpr bool PRIOR = true;    // the caller's bitmaps may come from the kernel before
-    struct Raw { uint2 w; };
-    __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
-        Raw r;
-        r.w = ok ? ldg_u2_l1(bits + (int64_t)row * words + (int64_t)kc * 2) : make_uint2(0u, 0u);
-        return r;
-    }
+    static constexpr int RAW = UM_BM * 16;
+    static constexpr bool DIRECT = false;
     template <int P>
     __device__ __forceinline__ static uint32_t pair(uint32_t w) {
         // bit P -> bit 15, bit P+16 -> bit 31; set bit -> +1 (0x3C00), clear -> -1 (0xBC00)
@@ -143,38 +114,51 @@ struct DecSign {
         o[8] = pair<8>(w);   o[9] = pair<9>(w);   o[10] = pair<10>(w); o[11] = pair<11>(w);
         o[12] = pair<12>(w); o[13] = pair<13>(w); o[14] = pair<14>(w); o[15] = pair<15>(w);
     }
-    __device__ __forceinline__ void decode(const Raw& r, uint32_t (&v)[32]) const {
-        word(r.w.x, v);
-        word(r.w.y, v + 16);
+    __device__ __forceinline__ static void issue(const CUtensorMap* m0, const CUtensorMap*, uint8_t* raw,
+                                                 uint64_t* bar, int row0, int kc) {
+        tma_load_2d(raw, m0, bar, (kc >> 1) * 4, row0);        // x in words
+    }
+    __device__ __forceinline__ static void decode(const uint8_t* raw, int r, int kc, uint32_t (&v)[32]) {
+        const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 16 + (kc & 1) * 8);
+        word(w.x, v);
+        word(w.y, v + 16);
     }
 };
 
 // Dense f16 rows, already in the K order the activations are staged in
-// (pair j of a stage = elements 2j, 2j+1): the decoder only moves them.  A
-// stage is 128 bytes per row, so one stage is loaded ahead.
+// (pair j of a stage = elements 2j, 2j+1): TMA loads them as the A operand.
 struct DecDense {
-    const uint16_t* rows;      // [rows][pitch] f16 bits
-    int64_t pitch;             // elements per row (a multiple of 64)
-    static constexpr int PF = 1;
-    static constexpr bool PRIOR = true;    // staged by the kernel before this one
-    struct Raw { uint4 q[8]; };
-    __device__ __forceinline__ Raw load(int row, bool ok, int kc) const {
-        Raw r;
-        const uint4* src = reinterpret_cast<const uint4*>(rows + (int64_t)row * pitch + (int64_t)kc * 64);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) r.q[i] = ok ? ldg_u4_l1(src + i) : make_uint4(0u, 0u, 0u, 0u);
-        return r;
+    static constexpr int RAW = 0;
+    static constexpr bool DIRECT = true;
+    __device__ __forceinline__ static void issue(const CUtensorMap* m0, const CUtensorMap*, uint8_t* a_stage,
+                                                 uint64_t* bar, int row0, int kc) {
+        tma_load_2d(a_stage, m0, bar, kc * UM_BK, row0);
     }
-    __device__ __forceinline__ void decode(const Raw& r, uint32_t (&v)[32]) const {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[4 * i] = r.q[i].x;
-            v[4 * i + 1] = r.q[i].y;
-            v[4 * i + 2] = r.q[i].z;
-            v[4 * i + 3] = r.q[i].w;
-        }
-    }
+    __device__ __forceinline__ static void decode(const uint8_t*, int, int, uint32_t (&)[32]) {}
 };
+
+// Host side: the tensor maps a plane's decoder loads from (PlaneMaps,
+// tq2_internal.h).
+// TQ2: codes [R][K/4] bytes; block-major scales [K/128][Rp] (Rp a multiple of 128)
+inline bool plane_maps_tq2(PlaneMaps& pm, const uint8_t* codes, const uint16_t* scales_t, int R, int K, int Rp) {
+    return make_tensor_map_2d(&pm.m0, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(codes), (uint64_t)K / 4,
+                              (uint64_t)R, (uint64_t)K / 4, 16u, (uint32_t)UM_BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_tensor_map_2d(&pm.m1, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<uint16_t*>(scales_t), (uint64_t)Rp,
+                              (uint64_t)K / 128, (uint64_t)Rp * 2, (uint32_t)UM_BM, 1u, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+// Sign: bits [R][K/32] u32 (K a multiple of 128)
+inline bool plane_maps_sign(PlaneMaps& pm, const uint32_t* bits, int R, int K) {
+    pm.m1 = CUtensorMap{};
+    return make_tensor_map_2d(&pm.m0, CU_TENSOR_MAP_DATA_TYPE_UINT32, const_cast<uint32_t*>(bits), (uint64_t)K / 32,
+                              (uint64_t)R, (uint64_t)K / 8, 4u, (uint32_t)UM_BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+// Dense: f16 rows [R][pitch] (pitch a multiple of 64)
+inline bool plane_maps_dense(PlaneMaps& pm, const uint16_t* rows, int R, int pitch) {
+    pm.m1 = CUtensorMap{};
+    return make_tensor_map_2d(&pm.m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<uint16_t*>(rows), (uint64_t)pitch,
+                              (uint64_t)R, (uint64_t)pitch * 2, (uint32_t)UM_BK, (uint32_t)UM_BM,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
 // --------------------------------------------------------------- epilogues ----
 enum EpiMode : int {
@@ -199,7 +183,7 @@ struct EpiArgs {
 // ----------------------------------------------------------------- kernel ----
 // Persistent: CTA b walks tiles b, b + gridDim.x, ...; tile t = (n-tile, token
 // tile, K split) with the n-tile fastest, so CTAs running together share one
-// activation tile in L2.  The stage ring and the two accumulators run
+// activation tile in L2.  The stage rings and the two accumulators run
 // continuously across tiles; the epilogue of a tile overlaps the MMAs of the
 // next.
 struct TileMap {
@@ -222,13 +206,15 @@ struct TileMap {
 // shared-memory round trip of the decoded rows would cost more than the MMAs.
 template <class Dec, int MODE, bool AT>
 __global__ void __launch_bounds__(UM_THREADS, 1)
-umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const EpiArgs ep, int T, int R, int BN,
-                 int tmem_cols, const TileMap tm, int S, int NACC, int cl) {
+umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap0,
+                 const __grid_constant__ CUtensorMap amap1, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
+                 const TileMap tm, int S, int SR, int NACC, int cl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stage_bytes = BN * 128;
     uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned (!AT)
-    UmmaBars* bars = reinterpret_cast<UmmaBars*>(a_ring + (AT ? 0 : S * UM_A_STAGE));
+    uint8_t* raw_ring = a_ring + (AT ? 0 : S * UM_A_STAGE);          // [SR][Dec::RAW] (!DIRECT)
+    UmmaBars* bars = reinterpret_cast<UmmaBars*>(raw_ring + (Dec::DIRECT ? 0 : SR * Dec::RAW));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
     // tiles of the same unit and share its activation tile: each loads 1/cl
@@ -243,6 +229,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             mbar_init(&bars->full_a[s], 4);
             mbar_init(&bars->empty[s], (uint32_t)cl);     // every cluster CTA's MMA must release it
         }
+        for (int r = 0; r < UM_RAW_STAGES; ++r) {
+            mbar_init(&bars->raw_full[r], 1);
+            mbar_init(&bars->raw_empty[r], 4);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->acc_full[b], 1);
             mbar_init(&bars->acc_empty[b], 4);
@@ -250,6 +240,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&amap0);
+        if (!Dec::DIRECT) tma_prefetch_desc(&amap1);
     }
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, (uint32_t)tmem_cols);
@@ -266,33 +258,60 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
     pdl_launch_dependents();
 
     if (warp == 0) {
-        if (lane == 0) {                                   // ---- TMA producer
+        if (lane == 0) {                                   // ---- activation TMA producer
             pdl_wait();
             int it = 0, s = 0;
             uint32_t ph = 0;                               // ring slot and phase parity of item `it`
             bool ok = true;
+            const uint32_t tx = (uint32_t)stage_bytes + (Dec::DIRECT ? (uint32_t)UM_A_STAGE : 0u);
             for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
+                const int row0 = (np * cl + rank) * UM_BM;
                 for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
                     if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->full_b[s], (uint32_t)stage_bytes);
+                    mbar_arrive_expect_tx(&bars->full_b[s], tx);
                     const int part = BN / cl;                  // token rows this CTA loads
                     if (cl > 1)
                         tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full_b[s], kc * UM_BK,
                                        m * BN + rank * part, cmask);
                     else
                         tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full_b[s], kc * UM_BK, m * BN);
+                    if (Dec::DIRECT) Dec::issue(&amap0, &amap1, a_ring + s * UM_A_STAGE, &bars->full_b[s], row0, kc);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
             // let the copies already issued land before the CTA can exit
             for (int i = (it > S ? it - S : 0); i < it; ++i)
                 mbar_wait(&bars->full_b[i % S], (uint32_t)(i / S) & 1u);
+        }
+    } else if (warp == 3) {
+        if (!Dec::DIRECT && lane == 0) {                   // ---- plane TMA producer (raw stages)
+            pdl_wait();
+            int it = 0, r = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
+                int np, m, z;
+                tm.decode(t, np, m, z);
+                const int row0 = (np * cl + rank) * UM_BM;
+                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
+                    if (it >= SR && !mbar_wait_or_abort(&bars->raw_empty[r], ph ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->raw_full[r], (uint32_t)Dec::RAW);
+                    Dec::issue(&amap0, &amap1, raw_ring + r * Dec::RAW, &bars->raw_full[r], row0, kc);
+                    if (++r == SR) { r = 0; ph ^= 1u; }
+                }
+            }
+            for (int i = (it > SR ? it - SR : 0); i < it; ++i)
+                mbar_wait(&bars->raw_full[i % SR], (uint32_t)(i / SR) & 1u);
         }
     } else if (warp == 1) {
         // ---- MMA issuer: the whole warp runs the loop, lane 0 waits on the
@@ -319,7 +338,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             const uint32_t dcol = tmem + (uint32_t)(buf * BN);
             const int k0 = tm.kc0(z), k1 = tm.kc1(z);
             for (int kc = k0; kc < k1; ++kc) {
-                if (!wait1(&bars->full_b[s], ph) || !wait1(&bars->full_a[s], ph)) {
+                if (!wait1(&bars->full_b[s], ph) || (!Dec::DIRECT && !wait1(&bars->full_a[s], ph))) {
                     if (lane == 0) *abort_flag = 1;
                     ok = false;
                     break;
@@ -348,89 +367,59 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
         }
     } else if (warp >= 4 && warp < 12) {                   // ---- decoders
-        // warp pair (q, h): lane quarter q, stages with item parity h
-        const int q = warp & 3, h = (warp - 4) >> 2;
-        const int arow = q * 32 + lane;                    // row of the A stage this thread writes
-        constexpr int PF = Dec::PF;                        // own items prefetched ahead
-        // flattened walk over this CTA's (tile, kc) items, two cursors
-        struct Cur {
-            int t, kc, k1, row;
-            bool rok;
-        };
-        auto start = [&](Cur& c, int t) {
-            c.t = t;
-            if (t < tm.total) {
+        if (!Dec::DIRECT) {
+            // warp pair (q, h): lane quarter q, stages with item parity h; a
+            // stage's raw tile is in shared memory (it landed S_R stages ahead)
+            const int q = warp & 3, h = (warp - 4) >> 2;
+            const int arow = q * 32 + lane;                // row of the tile this thread decodes
+            int it = 0, s = 0, r = 0;
+            uint32_t ph = 0, rph = 0;                      // A-ring and raw-ring phase parities of item `it`
+            bool ok = true;
+            for (int t = unit0; t < tm.total && ok; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
-                c.kc = tm.kc0(z);
-                c.k1 = tm.kc1(z);
-                c.row = (np * cl + rank) * UM_BM + q * 32 + lane;
-                c.rok = c.row < R;
+                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
+                    if ((it & 1) == h) {
+                        if (!mbar_wait_or_abort(&bars->raw_full[r], rph, abort_flag)) {
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        uint32_t v[32];
+                        Dec::decode(raw_ring + r * Dec::RAW, arow, kc, v);
+                        // the raw slot is refilled through the async proxy
+                        fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
+                        if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        if (AT) {
+                            // row arow = TMEM lane arow; pair j of the stage in column j of the stage's 32
+                            tc_fence_after();
+                            tmem_st_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)(s * (UM_BK / 2)),
+                                               v);
+                            tmem_wait_st();
+                            tc_fence_before();
+                        } else {
+                            // row arow of the stage: 16-byte chunk c (columns 4c..4c+3) at
+                            // chunk c ^ (arow & 7), the layout TMA would write with 128-byte swizzle
+                            uint8_t* rowp = a_ring + s * UM_A_STAGE + arow * 128;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(rowp + ((c ^ (arow & 7)) << 4)) =
+                                    make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                            fence_proxy_async_shared();    // the MMA reads A through the async proxy
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->full_a[s]);
+                    }
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                    if (++r == SR) { r = 0; rph ^= 1u; }
+                }
             }
-        };
-        auto step = [&](Cur& c) {
-            if (++c.kc >= c.k1) start(c, c.t + units);
-        };
-        Cur ld, pr;
-        if (Dec::PRIOR) pdl_wait();                        // the rows come from the previous kernel
-        start(ld, unit0);
-        start(pr, unit0);
-        int ld_it = 0;
-        typename Dec::Raw ring[PF];
-        // advance the load cursor to this warp's first item and prefetch PF items
-        auto next_own = [&](Cur& c, int& i) {
-            while (c.t < tm.total && (i & 1) != h) { step(c); ++i; }
-        };
-        next_own(ld, ld_it);
-#pragma unroll
-        for (int j = 0; j < PF; ++j) {
-            const bool live = ld.t < tm.total;
-            ring[j] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
-            if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
-        }
-        int it = 0, slot = 0, s = 0;
-        uint32_t ph = 0;                                   // ring slot and phase parity of item `it`
-        bool ok = true;
-        while (pr.t < tm.total && ok) {
-            if ((it & 1) == h) {
-                const typename Dec::Raw cur = ring[0];
-#pragma unroll
-                for (int j = 0; j + 1 < PF; ++j) ring[j] = ring[j + 1];
-                {
-                    const bool live = ld.t < tm.total;
-                    ring[PF - 1] = dec.load(live && ld.rok ? ld.row : 0, live && ld.rok, live ? ld.kc : 0);
-                    if (live) { step(ld); ++ld_it; next_own(ld, ld_it); }
-                }
-                if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                uint32_t v[32];
-                dec.decode(cur, v);
-                if (AT) {
-                    // row arow = TMEM lane arow; pair j of the stage in column j of the stage's 32
-                    tc_fence_after();
-                    tmem_st_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)(s * (UM_BK / 2)), v);
-                    tmem_wait_st();
-                    tc_fence_before();
-                } else {
-                    // row arow of the stage: 16-byte chunk c (columns 4c..4c+3) at
-                    // chunk c ^ (arow & 7), the layout TMA would write with 128-byte swizzle
-                    uint8_t* rowp = a_ring + s * UM_A_STAGE + arow * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(rowp + ((c ^ (arow & 7)) << 4)) =
-                            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                    fence_proxy_async_shared();            // the MMA reads A through the async proxy
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->full_a[s]);
-            }
-            step(pr);
-            ++it;
-            if (++s == S) { s = 0; ph ^= 1u; }
-            (void)slot;
         }
     } else if (warp >= 12) {                               // ---- epilogue
         const int q = warp & 3;
@@ -511,16 +500,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Dec dec, const 
 }
 
 // Host: launch one GEMM.  act16 is f16 [T][K] (row pitch K), staged in the
-// decoder's K order; R = plane rows; splits = K splits.  Token tiles of at
-// most 128 keep the decoded weights in tensor memory (AT) and run without
-// clusters; wider tiles decode into shared memory and pair CTAs on
-// neighbouring weight tiles to share the activation tile.
-template <class Dec, int MODE>
-cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN, int splits,
-                        cudaStream_t st);
-
+// decoder's K order; R = plane rows; splits = K splits; pm = the plane's
+// tensor maps.  Token tiles of at most 128 keep the decoded weights in
+// tensor memory (AT) and run without clusters; wider tiles decode into shared
+// memory and pair CTAs on neighbouring weight tiles to share the activation
+// tile.  Dense planes always take the shared-memory path (TMA writes A).
 template <class Dec, int MODE, bool AT>
-cudaError_t launch_umma_impl(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
+cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
     if (BN > UM_MAX_BN || BN % 16 != 0 || BN < 16 || (AT && BN > 128)) return cudaErrorInvalidValue;
     // the epilogue drains 32 columns at a time: a tile narrower than a
@@ -533,20 +519,32 @@ cudaError_t launch_umma_impl(const Dec& dec, const EpiArgs& ep, const void* act1
                             (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // two accumulators in tensor memory (the epilogue of a tile overlaps the
-    // next tile's MMAs); the B ring (and the A ring unless AT) fills the
-    // shared memory; with AT the A ring takes S x 32 tensor-memory columns
-    // after the accumulators (2 x 128 + 8 x 32 = 512 at most)
+    // next tile's MMAs); the B ring (and the A ring unless AT) in shared
+    // memory, then the raw plane ring with what is left; with AT the A ring
+    // takes S x 32 tensor-memory columns after the accumulators
+    // (2 x 128 + 8 x 32 = 512 at most)
     const int NACC = 2;
+    const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024;
     const int a_stage = AT ? 0 : UM_A_STAGE;
+    const int raw = Dec::DIRECT ? 0 : Dec::RAW;
     int S = UM_STAGES;
-    while (S > 2 && (size_t)S * (BN * 128 + a_stage) + sizeof(UmmaBars) + 1024 > (size_t)220 * 1024) --S;
+    // leave room for at least 8 raw stages
+    while (S > 2 && (size_t)S * (BN * 128 + a_stage) + (size_t)8 * raw > budget) --S;
+    int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (BN * 128 + a_stage)) / (size_t)(raw > 0 ? raw : 1));
+    if (SR > UM_RAW_STAGES) SR = UM_RAW_STAGES;
+    // an even depth: the two decoder warps of a quarter take alternate items,
+    // so items it and it + SR (one raw slot) belong to the same warp and no
+    // warp can wait on a slot's phase a ring round ahead of its filling
+    SR &= ~1;
+    if (SR < 2) return cudaErrorInvalidValue;
     int tmem_cols = 32;
     while (tmem_cols < NACC * BN + (AT ? S * (UM_BK / 2) : 0)) tmem_cols <<= 1;
     if (tmem_cols > 512) return cudaErrorInvalidValue;
     // At least 120 KB of shared memory: no two CTAs of this kernel can share
     // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
     // (which a cluster barrier could otherwise turn into a deadlock).
-    size_t smem = (size_t)S * (BN * 128 + a_stage) + 1024 + sizeof(UmmaBars) + 1024;
+    size_t smem = (size_t)S * (BN * 128 + a_stage) + (Dec::DIRECT ? 0 : (size_t)SR * raw) + 1024 + sizeof(UmmaBars) +
+                  1024;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
     tm.tiles_n = tiles_n;
@@ -576,15 +574,15 @@ cudaError_t launch_umma_impl(const Dec& dec, const EpiArgs& ep, const void* act1
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT>, xmap, dec, ep, T, R, BN, tmem_cols, tm, S, NACC,
-                              cl);
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols, tm,
+                              S, SR, NACC, cl);
 }
 
 template <class Dec, int MODE>
-cudaError_t launch_umma(const Dec& dec, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN, int splits,
-                        cudaStream_t st) {
-    if (BN <= 128) return launch_umma_impl<Dec, MODE, true>(dec, ep, act16, T, R, K, BN, splits, st);
-    return launch_umma_impl<Dec, MODE, false>(dec, ep, act16, T, R, K, BN, splits, st);
+cudaError_t launch_umma(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
+                        int splits, cudaStream_t st) {
+    if (BN <= 128 && !Dec::DIRECT) return launch_umma_impl<Dec, MODE, true>(pm, ep, act16, T, R, K, BN, splits, st);
+    return launch_umma_impl<Dec, MODE, false>(pm, ep, act16, T, R, K, BN, splits, st);
 }
 
 inline int umma_pick_bn(int T) {
