@@ -51,8 +51,7 @@ constexpr int BR_MAX_STAGES = 8;
 struct BrBars {
     uint64_t xfull[BR_MAX_STAGES];
     uint64_t xempty[BR_MAX_STAGES];
-    uint64_t full_a[BR_MAX_STAGES];
-    uint64_t full_b[BR_MAX_STAGES];
+    uint64_t full[BR_MAX_STAGES];    // a stage's A (8 converter warps) and B (4 decoder warps) are written
     uint64_t empty[BR_MAX_STAGES];
     uint64_t acc_full;
     uint32_t tmem_base;
@@ -109,8 +108,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
         for (int s = 0; s < S; ++s) {
             mbar_init(&bars->xfull[s], 1);
             mbar_init(&bars->xempty[s], 8);
-            mbar_init(&bars->full_a[s], 8);
-            mbar_init(&bars->full_b[s], 4);
+            mbar_init(&bars->full[s], 12);
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->acc_full, 1);
@@ -131,22 +129,23 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
     pdl_launch_dependents();
 
     if (warp == 0) {
-        // ---- MMA issuer (whole warp; lane 0 waits, an elected lane issues)
+        // ---- MMA issuer: the whole warp waits (one barrier a stage), the next
+        // stage's barrier is tested without blocking before this stage's MMAs,
+        // and an elected lane issues; the tensor pipe idles whenever this warp
+        // spends time between stages.
         const uint32_t idesc = idesc_f16_f32_bmn(128, (uint32_t)RB);
-        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            int r = 1;
-            if (lane == 0) r = mbar_wait_or_abort(bar, parity, abort_flag, true) ? 1 : 0;
-            return __shfl_sync(0xffffffffu, r, 0) != 0;
-        };
         int s = 0;
         uint32_t ph = 0;
-        bool ok = true;
+        bool ok = true, ready = false;
         for (int i = 0; i < nst; ++i) {
-            if (!wait1(&bars->full_a[s], ph) || !wait1(&bars->full_b[s], ph)) {
-                if (lane == 0) *abort_flag = 1;
+            if (!ready && !__all_sync(0xffffffffu, mbar_wait_or_abort(&bars->full[s], ph, abort_flag, true))) {
+                *abort_flag = 1;
                 ok = false;
                 break;
             }
+            const int s1 = s + 1 == S ? 0 : s + 1;
+            const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
+            ready = i + 1 < nst && mbar_test_wait(&bars->full[s1], ph1);
             tc_fence_after();
             const uint32_t bbase = smem_u32(bring + s * STAGE_B);
             const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (BR_BK / 2));
@@ -158,7 +157,9 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
                 umma_f16_ts_elect(tmem, acol + (uint32_t)(j * 8), bdesc, idesc, (i > 0 || j > 0) ? 1u : 0u);
             }
             umma_commit_elect(&bars->empty[s]);
-            if (++s == S) { s = 0; ph ^= 1u; }
+            s = s1;
+            ph = ph1;
+            ready = __all_sync(0xffffffffu, ready);
         }
         if (ok) umma_commit_elect(&bars->acc_full);
     } else if (warp == 2) {
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->full_a[s]);
+            if (lane == 0) mbar_arrive(&bars->full[s]);
         }
     } else if (warp >= 12) {
         // ---- decoders of the sign plane, then the accumulator drain
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             }
             fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->full_b[s]);
+            if (lane == 0) mbar_arrive(&bars->full[s]);
         }
         // drain: TMEM lane 32q + lane = token row of the tile
         if (nst > 0 && mbar_wait_or_abort(&bars->acc_full, 0u, abort_flag)) {

@@ -44,8 +44,7 @@ constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in share
 constexpr int UM_THREADS = 512;
 
 struct UmmaBars {
-    uint64_t full_b[UM_STAGES];
-    uint64_t full_a[UM_STAGES];
+    uint64_t full[UM_STAGES];      // a stage's B tile landed (TMA bytes) and its A rows are decoded (4 warps)
     uint64_t empty[UM_STAGES];
     uint64_t raw_full[UM_RAW_STAGES];
     uint64_t raw_empty[UM_RAW_STAGES];
@@ -225,8 +224,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < UM_STAGES; ++s) {
-            mbar_init(&bars->full_b[s], 1);
-            mbar_init(&bars->full_a[s], 4);
+            mbar_init(&bars->full[s], Dec::DIRECT ? 1u : 5u);   // TMA producer (+ the stage's 4 decoder warps)
             mbar_init(&bars->empty[s], (uint32_t)cl);     // every cluster CTA's MMA must release it
         }
         for (int r = 0; r < UM_RAW_STAGES; ++r) {
@@ -274,20 +272,20 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->full_b[s], tx);
+                    mbar_arrive_expect_tx(&bars->full[s], tx);
                     const int part = BN / cl;                  // token rows this CTA loads
                     if (cl > 1)
-                        tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full_b[s], kc * UM_BK,
+                        tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full[s], kc * UM_BK,
                                        m * BN + rank * part, cmask);
                     else
-                        tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full_b[s], kc * UM_BK, m * BN);
-                    if (Dec::DIRECT) Dec::issue(&amap0, &amap1, a_ring + s * UM_A_STAGE, &bars->full_b[s], row0, kc);
+                        tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full[s], kc * UM_BK, m * BN);
+                    if (Dec::DIRECT) Dec::issue(&amap0, &amap1, a_ring + s * UM_A_STAGE, &bars->full[s], row0, kc);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
             // let the copies already issued land before the CTA can exit
             for (int i = (it > S ? it - S : 0); i < it; ++i)
-                mbar_wait(&bars->full_b[i % S], (uint32_t)(i / S) & 1u);
+                mbar_wait(&bars->full[i % S], (uint32_t)(i / S) & 1u);
         }
     } else if (warp == 3) {
         if (!Dec::DIRECT && lane == 0) {                   // ---- plane TMA producer (raw stages)
@@ -314,35 +312,41 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 mbar_wait(&bars->raw_full[i % SR], (uint32_t)(i / SR) & 1u);
         }
     } else if (warp == 1) {
-        // ---- MMA issuer: the whole warp runs the loop, lane 0 waits on the
-        // barriers, and every MMA and commit is issued by one lane chosen with
-        // elect.sync, so the warp stays converged around the tcgen05 issue.
+        // ---- MMA issuer.  The tensor pipe holds about one MMA beyond the one
+        // executing, so whatever this warp does between two stages idles it:
+        // the whole warp waits (no lane-0 wait and broadcast), a stage has one
+        // barrier (B bytes and decoded A together), and the next stage's
+        // barrier is tested without blocking before this stage's MMAs are
+        // issued, so a stage that is already complete costs no wait at all.
+        // Every MMA and commit is issued by one lane chosen with elect.sync.
         const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
         int lt = 0, s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            int r = 1;
-            if (lane == 0) r = mbar_wait_or_abort(bar, parity, abort_flag, true) ? 1 : 0;
-            return __shfl_sync(0xffffffffu, r, 0) != 0;
+        bool ready = false;                                // full[s] of the next stage known complete
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {   // warp-uniform result
+            return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort_flag, true)) != 0;
         };
         for (int t = unit0; t < tm.total && ok; t += units, ++lt) {
             int np, m, z;
             tm.decode(t, np, m, z);
             const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
-            if (use >= 1 && !wait1(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u)) {
-                if (lane == 0) *abort_flag = 1;
+            if (use >= 1 && !wait_all(&bars->acc_empty[buf], (uint32_t)(use - 1) & 1u)) {
+                *abort_flag = 1;
                 break;
             }
             tc_fence_after();
             const uint32_t dcol = tmem + (uint32_t)(buf * BN);
             const int k0 = tm.kc0(z), k1 = tm.kc1(z);
             for (int kc = k0; kc < k1; ++kc) {
-                if (!wait1(&bars->full_b[s], ph) || (!Dec::DIRECT && !wait1(&bars->full_a[s], ph))) {
-                    if (lane == 0) *abort_flag = 1;
+                if (!ready && !wait_all(&bars->full[s], ph)) {
+                    *abort_flag = 1;
                     ok = false;
                     break;
                 }
+                const int s1 = s + 1 == S ? 0 : s + 1;
+                const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
+                ready = mbar_test_wait(&bars->full[s1], ph1);   // its latency hides under the MMAs below
                 tc_fence_after();
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
                 if (AT) {
@@ -360,7 +364,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 }
                 if (cl > 1) umma_commit_mc_elect(&bars->empty[s], cmask);
                 else umma_commit_elect(&bars->empty[s]);
-                if (++s == S) { s = 0; ph ^= 1u; }
+                s = s1;
+                ph = ph1;
+                ready = __all_sync(0xffffffffu, ready);
             }
             if (!ok) break;
             umma_commit_elect(&bars->acc_full[buf]);
@@ -414,7 +420,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             fence_proxy_async_shared();    // the MMA reads A through the async proxy
                         }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->full_a[s]);
+                        if (lane == 0) mbar_arrive(&bars->full[s]);
                     }
                     if (++s == S) { s = 0; ph ^= 1u; }
                     if (++r == SR) { r = 0; rph ^= 1u; }
