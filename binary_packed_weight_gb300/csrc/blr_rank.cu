@@ -13,8 +13,10 @@
 // not a multiple of 256) over a slice of K; the CL CTAs of a cluster take
 // the CL slices of the same tile and add their partial sums through
 // distributed shared memory in a fixed order (deterministic).  Roles:
-//   * one thread streams the f32 activation tile of each stage (128 tokens x
-//     64) into shared memory with TMA (two 32-column boxes, 128-byte swizzle);
+//   * one thread streams each stage's operands into shared memory: the f32
+//     activation tile (128 tokens x 64, two 32-column TMA boxes, 128-byte
+//     swizzle), the stage's 64 rows of sign words for the CTA's ranks (TMA)
+//     and the stage's 64 column factors (bulk copy);
 //   * eight converter warps (two per 32-token lane quarter, one per 32-column
 //     half of a stage) read their token's activations of every stage from
 //     there, multiply by the column vector and the scale, round to f16 and
@@ -49,8 +51,8 @@ constexpr int BR_BK = 64;              // K per stage
 constexpr int BR_MAX_STAGES = 8;
 
 struct BrBars {
-    uint64_t xfull[BR_MAX_STAGES];
-    uint64_t xempty[BR_MAX_STAGES];
+    uint64_t xfull[BR_MAX_STAGES];   // a stage's activations, sign words and column factors landed
+    uint64_t xempty[BR_MAX_STAGES];  // ... and have been read (8 converter + 4 decoder warps)
     uint64_t full[BR_MAX_STAGES];    // a stage's A (8 converter warps) and B (4 decoder warps) are written
     uint64_t empty[BR_MAX_STAGES];
     uint64_t acc_full;
@@ -83,16 +85,22 @@ __device__ __forceinline__ int br_rank_of(int n) {
 
 template <int RB>
 __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                 const __grid_constant__ CUtensorMap bmap,
                                                                  const BrArgs A, int S, int CL) {
     constexpr int STAGE_B = BR_BK * RB * 2;                 // B stage bytes (64 K rows x RB ranks f16)
     constexpr int STAGE_X = BR_BK * 128 * 4;                // activation stage bytes (128 tokens x 64 f32)
+    constexpr int STAGE_W = BR_BK * (RB / 32) * 4;          // sign words of a stage (64 rows x RB/32 words)
+    constexpr int STAGE_G = BR_BK * 4;                      // column factors of a stage
     constexpr int NA = RB / 64;                             // MN atoms a stage
     constexpr int RED_LD = RB + 4;                          // padded row of the drained partial (floats)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* bring = smem;                                  // [S][STAGE_B] sign-plane operand
     uint8_t* xring = smem + S * STAGE_B;                    // [S][STAGE_X] activation tiles
-    const int ring_bytes = S * (STAGE_B + STAGE_X) > 128 * RED_LD * 4 ? S * (STAGE_B + STAGE_X) : 128 * RED_LD * 4;
+    uint8_t* wring = xring + S * STAGE_X;                   // [S][STAGE_W] sign words
+    float* gring = reinterpret_cast<float*>(wring + S * STAGE_W);   // [S][64] column factors
+    const int used = S * (STAGE_B + STAGE_X + STAGE_W + STAGE_G);
+    const int ring_bytes = used > 128 * RED_LD * 4 ? used : 128 * RED_LD * 4;
     BrBars* bars = reinterpret_cast<BrBars*>(smem + ring_bytes + 16384);   // 16 KB guard after the rings
     float* red = reinterpret_cast<float*>(smem);            // [128][RED_LD], after the mainloop
 
@@ -102,12 +110,11 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
     const int nk = A.K / BR_BK;
     const int k0 = (int)(((int64_t)nk * z) / CL), k1 = (int)(((int64_t)nk * (z + 1)) / CL);
     const int nst = k1 - k0;
-    const int wpr = A.r / 32;                               // words of a bitmap row
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&bars->xfull[s], 1);
-            mbar_init(&bars->xempty[s], 8);
+            mbar_init(&bars->xempty[s], 12);
             mbar_init(&bars->full[s], 12);
             mbar_init(&bars->empty[s], 1);
         }
@@ -115,6 +122,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&bmap);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, 512u);
@@ -173,10 +181,12 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&bars->xfull[s], (uint32_t)STAGE_X);
+                mbar_arrive_expect_tx(&bars->xfull[s], (uint32_t)(STAGE_X + STAGE_W + STAGE_G));
                 const int kx = (k0 + i) * BR_BK;
                 tma_load_2d(xring + s * STAGE_X, &xmap, &bars->xfull[s], kx, tile * 128);
                 tma_load_2d(xring + s * STAGE_X + STAGE_X / 2, &xmap, &bars->xfull[s], kx + 32, tile * 128);
+                tma_load_2d(wring + s * STAGE_W, &bmap, &bars->xfull[s], rb * (RB / 32), kx);
+                bulk_load(gring + s * BR_BK, A.vec + kx, (uint32_t)STAGE_G, &bars->xfull[s]);
             }
         }
     } else if (warp >= 4 && warp < 12) {
@@ -187,11 +197,9 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
         const int q = warp & 3, h = (warp - 4) >> 2;
         const int i_row = q * 32 + lane;
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)(16 * h);
-        pdl_wait();                                         // the column vector may come from earlier work
         for (int i = 0; i < nst; ++i) {
             const int s = i % S;
             const uint32_t ph = (uint32_t)(i / S) & 1u;
-            const int kb = (k0 + i) * BR_BK + 32 * h;
             if (!mbar_wait_or_abort(&bars->xfull[s], ph, abort_flag)) {
                 *abort_flag = 1;
                 break;
@@ -202,11 +210,11 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             // into it comes through the async proxy.
             uint32_t w[16];
             const uint8_t* xr = xring + s * STAGE_X + h * (STAGE_X / 2) + i_row * 128;
-            const float4* vv = reinterpret_cast<const float4*>(A.vec + kb);
+            const float4* vv = reinterpret_cast<const float4*>(gring + s * BR_BK + 32 * h);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 v = *reinterpret_cast<const float4*>(xr + ((c ^ (i_row & 7)) << 4));
-                const float4 g = __ldg(vv + c);
+                const float4 g = vv[c];
                 const __half2 lo = __floats2half2_rn(v.x * g.x * A.scale, v.y * g.y * A.scale);
                 const __half2 hi = __floats2half2_rn(v.z * g.z * A.scale, v.w * g.w * A.scale);
                 w[2 * c] = *reinterpret_cast<const uint32_t*>(&lo);
@@ -229,18 +237,26 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
     } else if (warp >= 12) {
         // ---- decoders of the sign plane, then the accumulator drain
         const int q = warp & 3, tid = q * 32 + lane;      // 0..127
-        pdl_wait();
         constexpr int ITEMS = BR_BK * NA;                   // (row, 64-rank group) items a stage
         for (int i = 0; i < nst; ++i) {
             const int s = i % S;
             const uint32_t ph = (uint32_t)(i / S) & 1u;
-            const int kb = (k0 + i) * BR_BK;
+            if (!mbar_wait_or_abort(&bars->xfull[s], ph, abort_flag)) {
+                *abort_flag = 1;
+                break;
+            }
+            // item it = row j (fastest, so the 8 lanes of a 16-byte store phase
+            // write 8 different rows: 8 bank groups) x 64-rank group na
             uint2 wv[ITEMS / 128];
+            const uint32_t* wst = reinterpret_cast<const uint32_t*>(wring + s * STAGE_W);
 #pragma unroll
             for (int u = 0; u < ITEMS / 128; ++u) {
-                const int it = tid + 128 * u, j = it / NA, na = it % NA;
-                wv[u] = __ldg(reinterpret_cast<const uint2*>(A.bits + (int64_t)(kb + j) * wpr + rb * (RB / 32) + 2 * na));
+                const int it = tid + 128 * u, j = it % BR_BK, na = it / BR_BK;
+                wv[u] = *reinterpret_cast<const uint2*>(wst + j * (RB / 32) + 2 * na);
             }
+            fence_proxy_async_shared();                     // the slot is refilled through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xempty[s]);
             if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;
@@ -248,7 +264,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             uint8_t* stage = bring + s * STAGE_B;
 #pragma unroll
             for (int u = 0; u < ITEMS / 128; ++u) {
-                const int it = tid + 128 * u, j = it / NA, na = it % NA;
+                const int it = tid + 128 * u, j = it % BR_BK, na = it / BR_BK;
                 uint32_t c[32];
                 DecSign::word(wv[u].x, c);
                 DecSign::word(wv[u].y, c + 16);
@@ -386,9 +402,18 @@ template <int RB>
 cudaError_t br_launch(const BrArgs& a, int T, cudaStream_t st) {
     constexpr int STAGE_B = BR_BK * RB * 2;
     constexpr int STAGE_X = BR_BK * 128 * 4;
+    constexpr int STAGE_W = BR_BK * (RB / 32) * 4;
+    constexpr int STAGE_G = BR_BK * 4;
     const int S = RB == 256 ? 3 : 4;
     const int red_bytes = 128 * (RB + 4) * 4;
-    const int ring = S * (STAGE_B + STAGE_X) > red_bytes ? S * (STAGE_B + STAGE_X) : red_bytes;
+    const int used = S * (STAGE_B + STAGE_X + STAGE_W + STAGE_G);
+    const int ring = used > red_bytes ? used : red_bytes;
+    // the sign words [K][r/32] as RB/32-word x 64-row boxes
+    CUtensorMap bmap;
+    if (!make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, const_cast<uint32_t*>(a.bits), (uint64_t)a.r / 32,
+                            (uint64_t)a.K, (uint64_t)a.r / 8, (uint32_t)(RB / 32), (uint32_t)BR_BK,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     // the activation [T][K] f32 as 32-column x 128-token boxes, 128-byte swizzle
     CUtensorMap xmap;
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(a.act), (uint64_t)a.K,
@@ -419,7 +444,7 @@ cudaError_t br_launch(const BrArgs& a, int T, cudaStream_t st) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, blr_rank_kernel<RB>, xmap, a, S, CL);
+    return cudaLaunchKernelEx(&cfg, blr_rank_kernel<RB>, xmap, bmap, a, S, CL);
 }
 
 }  // namespace

@@ -482,11 +482,15 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         if (MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) colacc = fmaf(w, ep.other[o], colacc);
                     }
                 };
+                // both paths fully unrolled (a runtime index into v would put it
+                // in local memory); the full one without predicates
                 if (nvalid == 32) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) one(i);
                 } else {
-                    for (int i = 0; i < nvalid; ++i) one(i);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < nvalid) one(i);
                 }
             }
             if ((MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) && rok)
