@@ -29,11 +29,14 @@
 //     clear -> -1.0;
 //   * one warp issues tcgen05.mma (kind::f16, A from tensor memory, B from
 //     shared memory, f32 accumulation in tensor memory, N = RB);
-//   * the decoder warps then drain the accumulator into shared memory; after
-//     a cluster barrier CTA z sums rows [z*128/CL, (z+1)*128/CL) of the tile
-//     over the CL partials and writes the result, its f16 staging for the
-//     next GEMM, and (backward) the per-row-group partial column sums of
-//     result * other.
+//   * after a cluster barrier (every CTA's main loop is done, so every ring
+//     may be overwritten) the decoder warps drain the accumulator and store
+//     each row straight into the shared memory of the CTA that owns it (CTA z
+//     owns rows [z*128/CL, (z+1)*128/CL) of the tile), into a slot of its
+//     inbox per source CTA; after a second cluster barrier each CTA sums its
+//     inbox over the CL sources in a fixed order and writes the result, its
+//     f16 staging for the next GEMM, and (backward) the per-32-token partial
+//     column sums of result * other.
 // Within each 64-rank group the B operand holds ranks in the order the bits
 // fall out of a word: MN element 2p + h of the group is rank
 // (p < 16 ? 0 : 32) + p % 16 + 16 h.  That is also the order in which the
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
     const int used = S * (STAGE_B + STAGE_X + STAGE_W + STAGE_G);
     const int ring_bytes = used > 128 * RED_LD * 4 ? used : 128 * RED_LD * 4;
     BrBars* bars = reinterpret_cast<BrBars*>(smem + ring_bytes + 16384);   // 16 KB guard after the rings
-    float* red = reinterpret_cast<float*>(smem);            // [128][RED_LD], after the mainloop
+    float* red = reinterpret_cast<float*>(smem);            // inbox [CL][128/CL][RED_LD], after the main loops
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int z = (int)cluster_ctarank();                   // K slice = rank in the cluster
@@ -169,7 +172,12 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             ph = ph1;
             ready = __all_sync(0xffffffffu, ready);
         }
-        if (ok) umma_commit_elect(&bars->acc_full);
+        if (ok && nst > 0) {
+            umma_commit_elect(&bars->acc_full);
+            // every MMA must have finished reading this CTA's rings before the
+            // cluster barrier lets peers store into them
+            mbar_wait_or_abort(&bars->acc_full, 0u, abort_flag, true);
+        }
     } else if (warp == 2) {
         // ---- TMA producer of the activation tiles
         if (lane == 0) {
@@ -279,75 +287,104 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->full[s]);
         }
-        // drain: TMEM lane 32q + lane = token row of the tile
-        if (nst > 0 && mbar_wait_or_abort(&bars->acc_full, 0u, abort_flag)) {
-            tc_fence_after();
-            const uint32_t laddr = tmem + ((uint32_t)(q * 32) << 16);
-            float* rrow = red + (q * 32 + lane) * RED_LD;
-            for (int cc = 0; cc < RB; cc += 32) {
-                uint32_t v[32];
+    }
+
+    // every CTA of the cluster is past its main loop: the rings may be reused
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const int RPC = 128 / CL;                               // CL in {1, 2, 4}: a multiple of 32
+    if (warp >= 12) {
+        // drain: TMEM lane 32q + lane = token row of the tile, pushed to the
+        // owner CTA's inbox slot of this CTA (local when this CTA owns it)
+        const int q = warp & 3, row = q * 32 + lane;
+        const int owner = row / RPC, lr = row % RPC;
+        const uint32_t dst = mapa_shared(smem_u32(red + (z * RPC + lr) * RED_LD), (uint32_t)owner);
+        const bool have = nst > 0 && mbar_wait_or_abort(&bars->acc_full, 0u, abort_flag);
+        if (have) tc_fence_after();
+        const uint32_t laddr = tmem + ((uint32_t)(q * 32) << 16);
+        for (int cc = 0; cc < RB; cc += 32) {
+            uint32_t v[32];
+            if (have) {
                 tmem_ld_32x32b_x32(laddr + (uint32_t)cc, v);
                 tmem_wait_ld();
+            } else {                                        // no stage in this slice (or a wait gave up)
 #pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4)
-                    *reinterpret_cast<float4*>(rrow + cc + 4 * i4) =
-                        make_float4(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]),
-                                    __uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3]));
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
             }
-        } else {
-            // no stage in this slice (or a wait gave up): a zero partial
-            for (int rr = 0; rr < 32; ++rr)
-                for (int i = lane; i < RB; i += 32) red[(q * 32 + rr) * RED_LD + i] = 0.f;
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4)
+                st_dsmem_f4(dst + (uint32_t)((cc + 4 * i4) * 4),
+                            make_float4(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]),
+                                        __uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3])));
         }
     }
 
-    // every partial of the cluster is in shared memory
+    // every row is in its owner's inbox
     tc_fence_before();
     __syncthreads();
     cluster_sync();
 
-    // ---- reduction of rows [z*RPC, (z+1)*RPC) over the CL partials, in order.
-    // Warp w takes the 16 accumulator columns of segment w % NSEG and rows
-    // rgrp*32 + lane + p*32*ngrp of the CTA's share (rgrp = w / NSEG); each
-    // pass p covers one 32-token chunk, whose column sums of result * other
-    // are reduced over the lanes in a fixed butterfly order.
     pdl_wait();                                             // col, other: earlier work on the stream
     {
-        const int RPC = 128 / CL;                           // CL in {1, 2, 4}: a multiple of 32
         constexpr int NSEG = RB / 16;
         constexpr int NGRP = 16 / NSEG;
         const int seg = warp % NSEG, rgrp = warp / NSEG;
         const int n0 = seg * 16;                            // first accumulator column
         // the segment's 16 columns: ranks kA..kA+7 (even columns) and kA+16..kA+23 (odd)
         const int kA = rb * RB + (n0 >> 6) * 64 + br_rank_of(n0 & 63);
-        uint32_t base[4];
-        for (int zz = 0; zz < CL; ++zz) base[zz] = mapa_shared(smem_u32(red), (uint32_t)zz);
+        // the segment's column factors (ranks kA..kA+7, kA+16..kA+23)
+        float colv[16];
+        {
+            const float4 c0 = *reinterpret_cast<const float4*>(A.col + kA);
+            const float4 c1 = *reinterpret_cast<const float4*>(A.col + kA + 4);
+            const float4 c2 = *reinterpret_cast<const float4*>(A.col + kA + 16);
+            const float4 c3 = *reinterpret_cast<const float4*>(A.col + kA + 20);
+            const float cl[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
+                                  c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) colv[i] = cl[(i >> 1) + 8 * (i & 1)];
+        }
         for (int p = 0; rgrp * 32 + p * 32 * NGRP < RPC; ++p) {
-            const int row = z * RPC + rgrp * 32 + p * 32 * NGRP + lane;
+            const int lr = rgrp * 32 + p * 32 * NGRP + lane;     // row of this CTA's share
+            const int row = z * RPC + lr;
             const int t = tile * 128 + row;
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int zz = 0; zz < CL; ++zz) {
-                const uint32_t a = base[zz] + (uint32_t)((row * RED_LD + n0) * 4);
+            for (int zz = 0; zz < CL; ++zz) {                   // sources in order
+                const float4* src = reinterpret_cast<const float4*>(red + (zz * RPC + lr) * RED_LD + n0);
 #pragma unroll
                 for (int i4 = 0; i4 < 4; ++i4) {
-                    const float4 f = ld_dsmem_f4(a + 16u * i4);
+                    const float4 f = src[i4];
                     v[4 * i4] += f.x; v[4 * i4 + 1] += f.y; v[4 * i4 + 2] += f.z; v[4 * i4 + 3] += f.w;
                 }
             }
             const bool live = t < A.T;
             const int64_t rowoff = (int64_t)(live ? t : 0) * A.r;
-            float cs[16];
+            float cs[16], oth[16];
+            if (A.other && live) {
+                const float4 o0 = *reinterpret_cast<const float4*>(A.other + rowoff + kA);
+                const float4 o1 = *reinterpret_cast<const float4*>(A.other + rowoff + kA + 4);
+                const float4 o2 = *reinterpret_cast<const float4*>(A.other + rowoff + kA + 16);
+                const float4 o3 = *reinterpret_cast<const float4*>(A.other + rowoff + kA + 20);
+                const float ol[16] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w,
+                                      o2.x, o2.y, o2.z, o2.w, o3.x, o3.y, o3.z, o3.w};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) oth[i] = ol[(i >> 1) + 8 * (i & 1)];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) oth[i] = 0.f;
+            }
             __align__(16) uint16_t h16[16];
             __align__(16) float r0[8], r1[8];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float val = v[i] * A.oscale;
-                const int k = kA + (i >> 1) + 16 * (i & 1);
                 if (i & 1) r1[i >> 1] = val; else r0[i >> 1] = val;
-                h16[i] = __half_as_ushort(__float2half_rn(val * A.col[k] * A.scale2));
-                cs[i] = (A.other && live) ? val * A.other[rowoff + k] : 0.f;
+                h16[i] = __half_as_ushort(__float2half_rn(val * colv[i] * A.scale2));
+                cs[i] = val * oth[i];
             }
             if (live) {
                 if (A.res) {
@@ -386,10 +423,9 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
         }
     }
 
-    // peers may still read this CTA's partial: leave together
+    // nothing reads or writes another CTA's shared memory after the second barrier
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512u);

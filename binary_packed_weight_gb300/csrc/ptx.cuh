@@ -212,6 +212,11 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t cluster_addr) {
     return v;
 }
 
+__device__ __forceinline__ void st_dsmem_f4(uint32_t cluster_addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+
 // Bring the 128-byte line holding p into L2 ahead of its use.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
