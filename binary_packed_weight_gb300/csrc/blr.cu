@@ -203,13 +203,10 @@ int sm_count() {
     return sms;
 }
 
-// Token tile of the layer's GEMMs: at most 128 tokens, so the decoded sign
-// planes stay in tensor memory (the core's AT mode) and the activation tiles
-// are the only shared-memory operand.
-int blr_bn(int T) {
-    const int bn = umma_pick_bn(T);
-    return bn > 128 ? 128 : bn;
-}
+// Token tile of the layer's GEMMs: 256 tokens when there are enough (fewer
+// tiles, so fewer per-tile fills and drains; measured faster at T = 2048
+// than 128-token tiles with the sign plane in tensor memory), else all tokens.
+int blr_bn(int T) { return umma_pick_bn(T); }
 
 cudaError_t stage32(const float* src, const float* col, float scale, void* dst, int T, int Kd, cudaStream_t st) {
     const int64_t quarters = (int64_t)T * (Kd / 32) * 4;

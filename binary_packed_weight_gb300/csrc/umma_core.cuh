@@ -195,8 +195,10 @@ struct TileMap {
         m = rest % tiles_m;
         z = rest / tiles_m;
     }
-    __device__ __forceinline__ int kc0(int z) const { return (int)(((int64_t)nk_total * z) / splits); }
-    __device__ __forceinline__ int kc1(int z) const { return (int)(((int64_t)nk_total * (z + 1)) / splits); }
+    // 32-bit arithmetic (nk_total * splits < 2^31): a 64-bit division is a
+    // long software sequence on the GPU, paid on every tile by every role
+    __device__ __forceinline__ int kc0(int z) const { return (nk_total * z) / splits; }
+    __device__ __forceinline__ int kc1(int z) const { return (nk_total * (z + 1)) / splits; }
 };
 
 // AT: the decoded weights go to tensor memory (an S-stage ring of 32
