@@ -290,6 +290,38 @@ def extra_skinny(torch, bpw, stream, dev, pk, Ms):
     return res
 
 
+def extra_c3_sweep(torch, bpw, stream, dev, pk):
+    """Token-tile x K-split sweep of the tensor path at the batched-decode
+    shapes M = 32 and 128, N = 11008, K = 4096 (24 weight copies, > L2):
+    microseconds per GEMM (x staging included) for every tile and split
+    count, plus the library's own choice (bn 0, splits 0)."""
+    cfg = synth.SKINNY
+    N, K = cfg["N"], cfg["K"]
+    aos = synth.random_tq2(N, K, cfg["wkey"])
+    copies = 24
+    ws = [bpw.tq2_upload(aos, N, K) for _ in range(copies)]
+    res = {}
+    for M, tiles in ((32, (0, 32)), (128, (0, 32, 64, 128))):
+        x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+        row = {}
+        for bn in tiles:
+            for splits in ((0,) if bn == 0 else (1, 2, 4, 8)):
+                def step():
+                    for w in ws:
+                        bpw.tq2_gemm_tensor_tuned(w, x, out, bn, splits, stream=stream.cuda_stream)
+                n = reps(10)
+                secs, _ = time_graph(torch, step, n, 3, stream)
+                t = secs / (n * copies)
+                key = "auto" if bn == 0 else f"bn{bn}_k{splits}"
+                row[key] = dict(us=round(t * 1e6, 2), weight_gbs=round(gemv_bytes(N, K) / t / 1e9, 1),
+                                tflops=round(2.0 * M * N * K / t / 1e12, 1))
+        res[f"M{M}"] = row
+    for w in ws:
+        w.free()
+    return res
+
+
 def extra_blr(torch, bpw, stream, dev, pk):
     """blr layer forward + backward, T=2048 d_in=d_out=4096 r=512 (c recomputed)."""
     cfg = synth.BLR
@@ -650,6 +682,8 @@ def main():
             extra["tq2_dit_M1536_K3072"] = extra_dit(torch, bpw, stream, dev, pk)
         if not only or "quantize" in only:
             extra["tq2_quantize_N14336_K4096"] = extra_quantize(torch, bpw, stream, dev, pk)
+        if "c3sweep" in only:                     # on request only (a tuning table)
+            extra["tq2_c3_sweep_N11008"] = extra_c3_sweep(torch, bpw, stream, dev, pk)
 
     if rank != 0:
         return

@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path",
+    "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path", "tq2_gemm_tensor_tuned",
     "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths", "blr_sign_grads",
     "device_status", "debug_wait_timeout", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
@@ -35,6 +35,7 @@ _SIGS = {
     "tq2_shape": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "tq2_gemm": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "tq2_gemm_path": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P]),
+    "tq2_gemm_tensor_tuned": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "tq2_gemm_skinny_static": (_I, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "tq2_gemm_grouped": (_I, [_P, _P, _P, _I, _I64, _I64, _P]),
     "tq2_unpack": (_I, [_P, _P, _P]),
@@ -138,6 +139,14 @@ def tq2_gemm_path(w, x, out, path, stream=None):
     return out
 
 
+def tq2_gemm_tensor_tuned(w, x, out, bn=0, splits=0, stream=None):
+    """The tensor-core path with a chosen token tile (bn) and K-split count."""
+    M, K = x.shape
+    _check(load().tq2_gemm_tensor_tuned(w.handle, _ptr(x), _ptr(out), M, w.N, K, int(bn), int(splits),
+                                        _stream(stream)), "tq2_gemm_tensor_tuned")
+    return out
+
+
 def tq2_gemm_skinny_static(w, x, out, stream=None):
     """Skinny GEMM (M <= 16) that allocates nothing: its scratch is a fixed
     device array inside the library (see include/tq2.h)."""
@@ -148,7 +157,7 @@ def tq2_gemm_skinny_static(w, x, out, stream=None):
 
 
 def tq2_gemm_grouped(ws, xs, outs, stream=None):
-    """G independent GEMVs (M <= 2, same K) in one launch: outs[g] = xs[g] @ W_g^T."""
+    """G independent GEMVs (M <= 8, same K) in one launch: outs[g] = xs[g] @ W_g^T."""
     G = len(ws)
     M, K = xs[0].shape
     hs = (_P * G)(*[w.handle for w in ws])

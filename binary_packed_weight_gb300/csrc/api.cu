@@ -231,6 +231,35 @@ tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64_t M, in
     return fail(TQ2_EINVAL, "tq2_gemm: unknown path %d", path);
 }
 
+tq2_status tq2_gemm_tensor_tuned(tq2_handle h, const float* x, float* out, int64_t M, int64_t N, int64_t K,
+                                 int bn, int splits, void* stream) {
+    if (!h) return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: null handle");
+    if (M == 0) return TQ2_OK;
+    if (!x || !out) return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: null pointer");
+    if (M < 0 || M > (int64_t)1 << 24 || M * K >= (int64_t)1 << 31)
+        return fail(TQ2_ESHAPE, "tq2_gemm_tensor_tuned: bad M=%lld", (long long)M);
+    if (N != h->N || K != h->K)
+        return fail(TQ2_ESHAPE, "tq2_gemm_tensor_tuned: (N,K)=(%lld,%lld) but the handle holds (%lld,%lld)",
+                    (long long)N, (long long)K, (long long)h->N, (long long)h->K);
+    if ((reinterpret_cast<uintptr_t>(x) & 15) != 0)
+        return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: x must be 16-byte aligned");
+    // token tile: a multiple of 16 up to 256 (one that is not a multiple of
+    // 32 must cover all M tokens); K splits: 1..8 and at most K/64
+    if (bn != 0 && (bn < 16 || bn > 256 || bn % 16 != 0 || (bn % 32 != 0 && M > bn)))
+        return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: bad token tile %d", bn);
+    if (splits != 0 && (splits < 1 || splits > 8 || splits > K / 64))
+        return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: bad split count %d", splits);
+    cudaStream_t st = S(stream);
+    void* scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(&scratch, tq2::tensor_scratch_bytes(M, K), st);
+    if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm_tensor_tuned: scratch");
+    e = tq2::launch_tensor(h, x, out, (int)M, scratch, st, bn, splits);
+    cudaError_t e2 = cudaFreeAsync(scratch, st);
+    if (e != cudaSuccess) return cuda_fail(e, "tq2_gemm_tensor_tuned: launch");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "tq2_gemm_tensor_tuned: scratch free");
+    return TQ2_OK;
+}
+
 tq2_status tq2_gemm(tq2_handle h, const float* x, float* out, int64_t M, int64_t N, int64_t K, void* stream) {
     return tq2_gemm_path(h, x, out, M, N, K, TQ2_PATH_AUTO, stream);
 }
@@ -240,8 +269,10 @@ tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float*
     if (!hs || !xs || !outs) return fail(TQ2_EINVAL, "tq2_gemm_grouped: null array");
     if (G < 1 || G > tq2::GEMV_MAX_JOBS) return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= G <= %d", tq2::GEMV_MAX_JOBS);
     if (!tq2::gemv_supports((int)M, K))
-        return fail(TQ2_ESHAPE, "tq2_gemm_grouped: need 1 <= M <= %d and M*K <= %lld (M=%lld K=%lld)", tq2::GEMV_MAX_M,
-                    (long long)tq2::GEMV_MAX_MK, (long long)M, (long long)K);
+        return fail(TQ2_ESHAPE,
+                    "tq2_gemm_grouped: need 1 <= M <= %d and MT*K <= %lld, MT = M rounded up to 1, 2, 4 or 8 "
+                    "(M=%lld K=%lld)",
+                    tq2::GEMV_MAX_M, (long long)tq2::GEMV_MAX_MK, (long long)M, (long long)K);
     int64_t rows = 0;
     for (int g = 0; g < G; ++g) {
         const tq2_handle h = hs[g];

@@ -1,4 +1,4 @@
-// tq2_gemv.cu -- fused decode-shape GEMV for M <= 2 tokens.
+// tq2_gemv.cu -- fused decode-shape GEMV for M <= 8 tokens.
 //
 //   out[m,n] = sum_k x[m,k] * W[n,k],  W[n,k] = (c-1)*d   (BlockTQ2_0_g128,
 //   "oxibonsai-kernels 0.2.1, src/gpu_backend/metal_graph/tests_gemm_tq2.rs")
@@ -17,10 +17,13 @@
 //     never depend on earlier work on the stream, so this starts at once.
 //   * The consumers wait for the previous kernel (griddepcontrol.wait),
 //     convert x once into the hi/lo f16 B fragments of mma.m16n8k16 in
-//     shared memory, then per stage decode their 4 blocks (shift +
-//     mask|magic, see gv_pair) and issue the MMAs: one accumulator chain
-//     per block, four interleaved per warp, f32 accumulate, block scale
-//     applied to the block result d * (acc - correction).  The correction
+//     shared memory (B column 2m = token m's hi part, 2m+1 its lo part; M
+//     is padded to MT in {1, 2, 4, 8} tokens, so one n8 tile holds up to four
+//     tokens and MT = 8 takes two), then per stage decode their 4 blocks
+//     (shift + mask|magic, see gv_pair) and issue the MMAs -- each decoded
+//     A fragment feeds every n8 tile: one accumulator chain per block and
+//     tile, the blocks' chains interleaved per warp, f32 accumulate, block
+//     scale applied to the block result d * (acc - correction).  The correction
 //     sum_k (m_q+1) x_k of a block is computed by the very MMA chain that a
 //     block of all code-1 weights takes, so such a block gives exactly 0 and
 //     the rounding error of a block scales with its nonzero weights.
@@ -34,9 +37,10 @@
 //         over all of K, so no cross-warp reduction is needed.  Each warp
 //         keeps eight partial sums that mirror the k-split warps, so both
 //         ways give bit-identical results.
-// With few units per CTA, shared memory stays under ~110 KB so the next
-// kernel on the stream (launched early through programmatic dependent
-// launch) fits beside this one on every SM and streams its own weights.
+// Row-split launches keep shared memory under ~110 KB so that two CTAs share
+// an SM; k-split launches give their one CTA per SM all of it (a deeper
+// ring).  The next kernel on the stream is launched early (programmatic
+// dependent launch) and takes SM room as this grid's CTAs leave.
 #include "ptx.cuh"
 #include "tq2_internal.h"
 
@@ -58,6 +62,9 @@ constexpr int GV_SMEM_MAX = 225 * 1024;            // dynamic part; + up to 2 KB
 enum GvMode { GV_KSPLIT = 0, GV_ROWS = 1 };
 __host__ __device__ constexpr int gv_unit_rows(int mode) { return mode == GV_ROWS ? 16 * GV_CONS : 16; }
 __host__ __device__ constexpr int gv_stage_blocks(int mode) { return mode == GV_ROWS ? GV_BPW : GV_BPW * GV_CONS; }
+// tokens padded to MT in {1, 2, 4, 8}; B columns 2MT in one or two n8 tiles
+__host__ __device__ constexpr int gv_mt(int M) { return M <= 2 ? M : (M <= 4 ? 4 : 8); }
+__host__ __device__ constexpr int gv_tiles(int MT) { return MT > 4 ? 2 : 1; }
 
 struct GemvJob {
     CUtensorMap map;              // the weight's code-plane map for the launch's mode
@@ -72,6 +79,7 @@ struct GemvTab {
     GemvJob job[NJ];
     int njobs;
     int K;
+    int M;                        // tokens (<= MT; the rest of the MT columns are zero)
 };
 
 // The per-job fields the loops read, copied to shared memory once: the job
@@ -161,7 +169,7 @@ __host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stage
     L.nch = (L.nb + gv_stage_blocks(mode) - 1) / gv_stage_blocks(mode);
     L.off_red = 512;                                                   // full, empty, sfull, sempty
     L.off_corr = L.off_red + (mode == GV_KSPLIT ? 2u * GV_CONS * 16 * MT * 4 : 0u);
-    L.off_sc = L.off_corr + (((uint32_t)L.nb + 3u) & ~3u) * MT * 4;             // whole pieces (float4 reads)
+    L.off_sc = L.off_corr + (((uint32_t)L.nb + 3u) & ~3u) * MT * 4;             // [MT][nb rounded to 4] (float4 reads)
     L.sc_bytes = ((uint32_t)gv_unit_rows(mode) * L.nb * 2 + 16u + 15u) & ~15u;
     L.off_xs = L.off_sc + (uint32_t)sslots * L.sc_bytes;
     // [nb rounded up to whole pieces][4 step pairs][2MT][4] uint4
@@ -177,14 +185,17 @@ __host__ __device__ inline GvLayout gv_layout(int K, int MT, int mode, int stage
 // row g's scales (row g+8's are 8*nb further).  x fragments are stored
 // [block][k16 step pair][column][t] (uint4 = two steps' b0,b1), so the
 // lanes of one load read 16 * 8 * MT contiguous bytes; xl is this lane's
-// fragment base, xstep / sstep its strides per block / step pair.  Lanes
-// g >= 2MT supply B columns whose D columns are never read, so they load
-// another lane's fragment (a broadcast).  Each block's eight MMAs form one
-// accumulator chain; the four blocks' chains interleave.
+// fragment base in n8 tile 0 (tile 1, columns 8..15, is 32 uint4 further),
+// xstep / sstep its strides per block / step pair.  Lanes g >= 2MT supply B
+// columns whose D columns are never read, so they load another lane's
+// fragment (a broadcast).  cr points at the corrections of this lane's
+// token of tile 0 (tile 1's token, 4 later, is 4*nbp further).  Each block
+// and tile's eight MMAs form one accumulator chain; the chains interleave.
 template <int MT, bool FULL>
 __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const uint4* xl, int xstep, int sstep,
-                                         const float* corr, int blk0, int nv, int nb, const uint16_t* scA, int tm,
-                                         const GvShift& sh, float& totA, float& totB) {
+                                         const float* cr, int nbp, int blk0, int nv, int nb, const uint16_t* scA,
+                                         const GvShift& sh, float (&totA)[gv_tiles(MT)], float (&totB)[gv_tiles(MT)]) {
+    constexpr int NT = gv_tiles(MT);
     uint32_t wa[GV_BPW][2][3], wb[GV_BPW][2][3];
     const uint4* xb = xl + blk0 * xstep;
 #pragma unroll
@@ -197,20 +208,23 @@ __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const 
         gv_word(cb.x, sh, wb[i][0]);
         gv_word(cb.y, sh, wb[i][1]);
     }
-    float acc[GV_BPW][4];
+    float acc[GV_BPW][NT][4];
 #pragma unroll
     for (int i = 0; i < GV_BPW; ++i)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
     // steps 0-3 decode word x (k 32t..32t+15 of the block), 4-7 word y
 #define GV_STEP2(S)                                                                         \
     _Pragma("unroll") for (int i = 0; i < GV_BPW; ++i) {                                    \
-        const uint4 b = xb[i * xstep + ((S) / 2) * sstep];                                  \
+        uint4 b[NT];                                                                        \
+        _Pragma("unroll") for (int j = 0; j < NT; ++j) b[j] = xb[i * xstep + ((S) / 2) * sstep + 32 * j]; \
         uint32_t a[4];                                                                      \
         gv_afrag<(S) % 4>(wa[i][(S) / 4], wb[i][(S) / 4], a, sh);                           \
-        mma_16816_pure(acc[i], a, b.x, b.y);                                                \
+        _Pragma("unroll") for (int j = 0; j < NT; ++j) mma_16816_pure(acc[i][j], a, b[j].x, b[j].y); \
         gv_afrag<((S) + 1) % 4>(wa[i][(S) / 4], wb[i][(S) / 4], a, sh);                     \
-        mma_16816_pure(acc[i], a, b.z, b.w);                                                \
+        _Pragma("unroll") for (int j = 0; j < NT; ++j) mma_16816_pure(acc[i][j], a, b[j].z, b[j].w); \
     }
     GV_STEP2(0)
     GV_STEP2(2)
@@ -218,7 +232,7 @@ __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const 
     GV_STEP2(6)
 #undef GV_STEP2
     // block scales (f16) and corrections of the four blocks
-    float dA[GV_BPW], dB[GV_BPW], cr[GV_BPW];
+    float dA[GV_BPW], dB[GV_BPW];
     if ((nb & 3) == 0) {
         const uint2 ua = *reinterpret_cast<const uint2*>(scA + blk0);
         const uint2 ub = *reinterpret_cast<const uint2*>(scA + 8 * nb + blk0);
@@ -235,36 +249,34 @@ __device__ __forceinline__ void gv_piece(const uint8_t* pc, int g, int t, const 
             dB[i] = __half2float(__ushort_as_half(scA[8 * nb + blk0 + i]));
         }
     }
-    {
-        const float4* c4 = reinterpret_cast<const float4*>(corr + blk0 * MT);
-        float cv[GV_BPW * MT];
 #pragma unroll
-        for (int q = 0; q < MT; ++q) {
-            const float4 v = c4[q];
-            cv[4 * q] = v.x; cv[4 * q + 1] = v.y; cv[4 * q + 2] = v.z; cv[4 * q + 3] = v.w;
-        }
+    for (int j = 0; j < NT; ++j) {
+        const float4 c = *reinterpret_cast<const float4*>(cr + 4 * j * nbp + blk0);
+        const float cv[GV_BPW] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int i = 0; i < GV_BPW; ++i) cr[i] = (MT == 1 || tm == 0) ? cv[i * MT] : cv[i * MT + MT - 1];
-    }
-#pragma unroll
-    for (int i = 0; i < GV_BPW; ++i) {
-        if (FULL || i < nv) {
-            totA = fmaf(dA[i], (acc[i][0] + acc[i][1]) - cr[i], totA);
-            totB = fmaf(dB[i], (acc[i][2] + acc[i][3]) - cr[i], totB);
+        for (int i = 0; i < GV_BPW; ++i) {
+            if (FULL || i < nv) {
+                totA[j] = fmaf(dA[i], (acc[i][j][0] + acc[i][j][1]) - cv[i], totA[j]);
+                totB[j] = fmaf(dB[i], (acc[i][j][2] + acc[i][j][3]) - cv[i], totB[j]);
+            }
         }
     }
 }
 
 }  // namespace
 
-// Registers: row-split launches run two CTAs per SM, and 18 warps spread over
-// four 16K-register sub-partitions fit only at <= 96 registers a thread;
-// k-split launches keep one CTA per SM (plus the next kernel's, when it fits)
-// and take 112.
+// Registers: two CTAs per SM (18 warps spread over four 16K-register
+// sub-partitions) fit only at <= 96 registers a thread.  Four tokens in a
+// k-split launch (64 KB of x, one CTA per SM) take 112 and two n8 tiles 128
+// (with 128 KB of x).
+__host__ __device__ constexpr int gv_maxnreg(int MT, int mode) {
+    return gv_tiles(MT) == 2 ? 128 : (mode == GV_KSPLIT && MT == 4 ? 112 : 96);
+}
 template <int MT, int MODE, int NJ>
-__global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __grid_constant__ GemvTab<NJ> tab, int units, int stages,
-                                                 int sslots) {
+__global__ void __maxnreg__(gv_maxnreg(MT, MODE))
+    tq2_gemv_kernel(const __grid_constant__ GemvTab<NJ> tab, int units, int stages, int sslots) {
     constexpr int UR = gv_unit_rows(MODE);
+    constexpr int NT = gv_tiles(MT);
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ GvJobS sj[NJ];
     const GvLayout L = gv_layout(tab.K, MT, MODE, stages, sslots);
@@ -274,14 +286,15 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
     uint64_t* sfull = empty + GV_MAX_STAGES;
     uint64_t* sempty = sfull + GV_MAX_SSLOTS;
     float* red = reinterpret_cast<float*>(smem + L.off_red);       // [2][GV_CONS][16][MT] (k-split)
-    float* corr = reinterpret_cast<float*>(smem + L.off_corr);     // [nb][MT]
+    float* corr = reinterpret_cast<float*>(smem + L.off_corr);     // [MT][nbp]
     uint8_t* scb = smem + L.off_sc;                                // [sslots] x ([UR][nb] f16)
     uint2* xs = reinterpret_cast<uint2*>(smem + L.off_xs);         // [nb][4][2MT][4][2]
     // [stages][8 warps][16 rows][128 B], 1 KB aligned for the 128-byte swizzle
     uint8_t* ring = smem + L.off_ring + ((1024u - ((smem_u32(smem) + L.off_ring) & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nb = L.nb, nch = L.nch, K = tab.K;
+    const int nb = L.nb, nch = L.nch, K = tab.K, Mr = tab.M;
+    const int nbp = (nb + 3) & ~3;
     const int u_begin = (int)(((int64_t)blockIdx.x * units) / gridDim.x);
     const int u_end = (int)(((int64_t)(blockIdx.x + 1) * units) / gridDim.x);
 
@@ -352,7 +365,8 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
 
     // ---------------------------------------------------- consumer warps ----
     const int g = lane >> 2, t = lane & 3;
-    const int tm = t < MT ? t : MT - 1;          // token of this lane's D columns 2t, 2t+1 (if t < MT)
+    const int tm = t < MT ? t : MT - 1;          // token of this lane's D columns 2t, 2t+1 in tile 0 (if t < MT)
+    const float* cr = corr + tm * nbp;
     // staging role of this lane: block (lane / 8) of the pass, word pair t, half y
     const int st_q = lane >> 3, st_t = (lane >> 1) & 3, st_y = lane & 1;
     // x blocks this warp converts: k-split -- the ones it uses,
@@ -395,25 +409,38 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
             const int blk = MODE == GV_KSPLIT ? (li / GV_BPW) * (GV_BPW * GV_CONS) + GV_BPW * warp + li % GV_BPW
                                               : warp + GV_CONS * li;
             const int k0 = (live ? blk : 0) * 128 + 32 * st_t + 16 * st_y;
+            // tokens in batches of SB: all of a batch's loads are issued
+            // before any is converted, so a batch costs one L2 round trip
+            constexpr int SB = MT == 8 && MODE == GV_KSPLIT ? 4 : (MT >= 2 && gv_maxnreg(MT, MODE) > 96 ? 2 : 1);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float e[16];
-                const float4* src = reinterpret_cast<const float4*>(x + (int64_t)m * K + k0);
+            for (int m0 = 0; m0 < MT; m0 += SB) {
+                float4 q[SB][4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 q = live ? __ldg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    e[4 * v] = q.x; e[4 * v + 1] = q.y; e[4 * v + 2] = q.z; e[4 * v + 3] = q.w;
+                for (int mb = 0; mb < SB; ++mb) {
+                    const int m = m0 + mb;
+                    const float4* src = reinterpret_cast<const float4*>(x + (int64_t)m * K + k0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        q[mb][v] = live && m < Mr ? __ldg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 if (live) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {               // k16 step 4y + j: pairs 2j, 2j+1
-                        uint32_t h01, l01, h23, l23;
-                        split2(e[2 * j], e[2 * j + 8], h01, l01);
-                        split2(e[2 * j + 1], e[2 * j + 9], h23, l23);
-                        // step 4y + j -> pair 2y + j/2, half j % 2
-                        uint2* d = xs + (((blk * 4 + 2 * st_y + (j >> 1)) * (2 * MT) + 2 * m) * 4 + st_t) * 2 + (j & 1);
-                        d[0] = make_uint2(h01, h23);              // column 2m: hi
-                        d[8] = make_uint2(l01, l23);              // column 2m+1: lo
+                    for (int mb = 0; mb < SB; ++mb) {
+                        const int m = m0 + mb;
+                        const float e[16] = {q[mb][0].x, q[mb][0].y, q[mb][0].z, q[mb][0].w,
+                                             q[mb][1].x, q[mb][1].y, q[mb][1].z, q[mb][1].w,
+                                             q[mb][2].x, q[mb][2].y, q[mb][2].z, q[mb][2].w,
+                                             q[mb][3].x, q[mb][3].y, q[mb][3].z, q[mb][3].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {           // k16 step 4y + j: pairs 2j, 2j+1
+                            uint32_t h01, l01, h23, l23;
+                            split2(e[2 * j], e[2 * j + 8], h01, l01);
+                            split2(e[2 * j + 1], e[2 * j + 9], h23, l23);
+                            // step 4y + j -> pair 2y + j/2, half j % 2
+                            uint2* d = xs + (((blk * 4 + 2 * st_y + (j >> 1)) * (2 * MT) + 2 * m) * 4 + st_t) * 2 + (j & 1);
+                            d[0] = make_uint2(h01, h23);          // column 2m: hi
+                            d[8] = make_uint2(l01, l23);          // column 2m+1: lo
+                        }
                     }
                 }
             }
@@ -423,19 +450,38 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
         // Corrections sum_k (m_q+1) x_k per block and token: the MMA chain of
         // gv_piece (same steps, same order, accumulator from zero) on a row of
         // all code-1 weights, so that d * (acc - correction) is exactly 0 for
-        // such a block.  Each warp takes the blocks it staged.
-        for (int li = 0; li < nbw; ++li) {
-            const int blk = MODE == GV_KSPLIT ? (li / GV_BPW) * (GV_BPW * GV_CONS) + GV_BPW * warp + li % GV_BPW
-                                              : warp + GV_CONS * li;
-            const uint4* xb = xl + blk * xstep;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // such a block.  Each warp takes the blocks it staged, CI chains at a
+        // time, interleaved (fewer where registers are scarce).
+        constexpr int CI = MT >= 2 && gv_maxnreg(MT, MODE) <= 96 ? (MODE == GV_KSPLIT ? 1 : 2) : 4;
+        for (int l0 = 0; l0 < nbw; l0 += CI) {
+            int blk[CI];
+            float acc[CI][NT][4];
+#pragma unroll
+            for (int i = 0; i < CI; ++i) {
+                const int li = min(l0 + i, nbw - 1);              // past the end: repeat the last block
+                blk[i] = MODE == GV_KSPLIT ? (li / GV_BPW) * (GV_BPW * GV_CONS) + GV_BPW * warp + li % GV_BPW
+                                           : warp + GV_CONS * li;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+            }
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const uint4 b = xb[p * sstep];
-                mma_16816_pure(acc, ones[(2 * p) & 3], b.x, b.y);
-                mma_16816_pure(acc, ones[(2 * p + 1) & 3], b.z, b.w);
+#pragma unroll
+                for (int i = 0; i < CI; ++i) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const uint4 b = xl[blk[i] * xstep + p * sstep + 32 * j];
+                        mma_16816_pure(acc[i][j], ones[(2 * p) & 3], b.x, b.y);
+                        mma_16816_pure(acc[i][j], ones[(2 * p + 1) & 3], b.z, b.w);
+                    }
+                }
             }
-            if (g == 0 && t < MT) corr[blk * MT + t] = acc[0] + acc[1];
+            if (g == 0 && t < MT) {
+#pragma unroll
+                for (int i = 0; i < CI; ++i)
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) corr[(t + 4 * j) * nbp + blk[i]] = acc[i][j][0] + acc[i][j][1];
+            }
         }
         if (MODE == GV_ROWS) consumers_sync();                // every correction written
         else __syncwarp();
@@ -453,18 +499,20 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
         if (J.x != staged) stage_x(J.x);
         if (!dead && !mbar_wait(&sfull[slot], sph)) dead = true;
         const uint16_t* scA = reinterpret_cast<const uint16_t*>(scb + slot * L.sc_bytes) + (rbase + g) * nb;
-        auto do_stage = [&](int c, float& ta, float& tb) {
+        auto do_stage = [&](int c, float (&ta)[NT], float (&tb)[NT]) {
             if (!dead && !mbar_wait(&full[s], ph)) dead = true;   // after a timeout: no more waits
             const uint8_t* pc = ring + s * GV_STAGE + warp * GV_WARP_BYTES + g * GV_PIECE + 8 * (t & 1);
             const int blk0 = MODE == GV_ROWS ? GV_BPW * c : c * (GV_BPW * GV_CONS) + GV_BPW * warp;
             const int nv = min(GV_BPW, nb - blk0);              // valid blocks (warp-uniform)
-            if (nv == GV_BPW) gv_piece<MT, true>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
-            else if (nv > 0) gv_piece<MT, false>(pc, g, t, xl, xstep, sstep, corr, blk0, nv, nb, scA, tm, sh, ta, tb);
+            if (nv == GV_BPW) gv_piece<MT, true>(pc, g, t, xl, xstep, sstep, cr, nbp, blk0, nv, nb, scA, sh, ta, tb);
+            else if (nv > 0) gv_piece<MT, false>(pc, g, t, xl, xstep, sstep, cr, nbp, blk0, nv, nb, scA, sh, ta, tb);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (++s == stages) { s = 0; ph ^= 1u; }
         };
-        float totA = 0.f, totB = 0.f;            // rows rbase+g and rbase+g+8, token tm
+        float totA[NT], totB[NT];                // rows rbase+g and rbase+g+8; tokens tm, tm + 4
+#pragma unroll
+        for (int j = 0; j < NT; ++j) totA[j] = totB[j] = 0.f;
         if (MODE == GV_KSPLIT) {
             for (int c = 0; c < nch; ++c) do_stage(c, totA, totB);
         } else {
@@ -475,10 +523,15 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
             // same order as the k-split reduction.  One partial pair is live
             // at a time instead of eight.
             for (int j = 0; j < GV_CONS; ++j) {
-                float pa = 0.f, pb = 0.f;
+                float pa[NT], pb[NT];
+#pragma unroll
+                for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0.f;
                 for (int c = j; c < nch; c += GV_CONS) do_stage(c, pa, pb);
-                totA += pa;
-                totB += pb;
+#pragma unroll
+                for (int q = 0; q < NT; ++q) {
+                    totA[q] += pa[q];
+                    totB[q] += pb[q];
+                }
             }
         }
         __syncwarp();
@@ -489,14 +542,23 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
         if (MODE == GV_ROWS) {
             if (t < MT) {
                 const int ra = n0 + rbase + g;
-                if (ra < J.N) J.out[(int64_t)t * J.N + ra] = totA;
-                if (ra + 8 < J.N) J.out[(int64_t)t * J.N + ra + 8] = totB;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int m = t + 4 * j;
+                    if (m < Mr) {
+                        if (ra < J.N) J.out[(int64_t)m * J.N + ra] = totA[j];
+                        if (ra + 8 < J.N) J.out[(int64_t)m * J.N + ra + 8] = totB[j];
+                    }
+                }
             }
         } else {
             float* rd = red + (ui & 1) * (GV_CONS * 16 * MT);
             if (t < MT) {
-                rd[(warp * 16 + g) * MT + t] = totA;
-                rd[(warp * 16 + g + 8) * MT + t] = totB;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    rd[(warp * 16 + g) * MT + t + 4 * j] = totA[j];
+                    rd[(warp * 16 + g + 8) * MT + t + 4 * j] = totB[j];
+                }
             }
             consumers_sync();
             if ((int)threadIdx.x < 16 * MT) {
@@ -504,7 +566,7 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
                 float sum = 0.f;
 #pragma unroll
                 for (int w = 0; w < GV_CONS; ++w) sum += rd[(w * 16 + r) * MT + m];
-                if (n0 + r < J.N) J.out[(int64_t)m * J.N + n0 + r] = sum;
+                if (m < Mr && n0 + r < J.N) J.out[(int64_t)m * J.N + n0 + r] = sum;
             }
         }
     }
@@ -512,17 +574,20 @@ __global__ void __maxnreg__(MODE == GV_ROWS ? 96 : 112) tq2_gemv_kernel(const __
 
 namespace {
 
-// Ring depth and scale slots for a mode: as many stages as fit beside a
-// second CTA (else alone); enough scale slots that the code ring, not the
-// scales, limits how far the producer runs ahead.  False if nothing fits.
-bool gv_plan(int K, int MT, int mode, int& stages, int& sslots) {
+// Ring depth and scale slots: with `pair`, as many stages as fit beside a
+// second CTA of the grid (false below four); else all of an SM's shared
+// memory, which also keeps the next kernel's CTAs (launched early) off the SM
+// until this grid's CTA leaves -- early CTAs that doubled up on SMs a
+// one-per-SM grid left idle made chained GEMVs slower.  Enough scale slots
+// that the code ring, not the scales, limits how far the producer runs
+// ahead.  False if nothing fits.
+bool gv_plan(int K, int MT, int mode, bool pair, int& stages, int& sslots) {
     sslots = 2;
     for (int pass = 0; pass < 2; ++pass) {
         const int fixed = (int)gv_layout(K, MT, mode, 0, sslots).total;
-        stages = (GV_SMEM_PAIR - fixed) / GV_STAGE;
-        if (stages < 4) stages = (GV_SMEM_MAX - fixed) / GV_STAGE;
+        stages = ((pair ? GV_SMEM_PAIR : GV_SMEM_MAX) - fixed) / GV_STAGE;
         if (stages > GV_MAX_STAGES) stages = GV_MAX_STAGES;
-        if (stages < 2) return false;
+        if (stages < (pair ? 4 : 2)) return false;
         if (pass == 0) {
             const int nch = (K / 128 + gv_stage_blocks(mode) - 1) / gv_stage_blocks(mode);
             sslots = (stages + nch - 1) / nch + 1;
@@ -547,13 +612,14 @@ cudaError_t gv_launch(const GemvTab<NJ>& tab, int units, int stages, int sslots,
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    // k-split: at most one CTA per SM while that leaves each only a few units
-    // (the next kernel on the stream then fits beside it); otherwise two per
-    // SM, since eight consumer warps alone do not hide the MMA and load latency.
-    const int slots = (MODE == GV_ROWS || units >= 8 * sms) ? 2 * sms : sms;
-    const int per = (units + slots - 1) / slots;
-    const int grid = (units + per - 1) / per;
+    // two CTAs per SM where the plan leaves room (eight consumer warps alone
+    // do not hide the MMA and load latency), else one; every slot gets work
+    // (units split as evenly as the count allows), so no SM is left for the
+    // next kernel's early CTAs to double up on
     const GvLayout L = gv_layout(tab.K, MT, MODE, stages, sslots);
+    const bool pair = L.total + 2048u <= (uint32_t)GV_SMEM_PAIR && gv_maxnreg(MT, MODE) <= 96;   // two CTAs fit
+    const int slots = pair ? 2 * sms : sms;
+    const int grid = units < slots ? units : slots;
     return launch_pdl(tq2_gemv_kernel<MT, MODE, NJ>, dim3((unsigned)grid), dim3(GV_THREADS), (size_t)L.total, st,
                       tab, units, stages, sslots);
 }
@@ -568,14 +634,22 @@ cudaError_t gv_dispatch(const tq2_weight* const* ws, const float* const* xs, flo
     const int K = (int)ws[0]->K;
     int64_t units_r = 0;
     for (int g = 0; g < G; ++g) units_r += (ws[g]->N + gv_unit_rows(GV_ROWS) - 1) / gv_unit_rows(GV_ROWS);
+    const int MT = gv_mt(M);
     int stages = 0, sslots = 0;
     int mode = GV_KSPLIT;
-    if (units_r >= sms && gv_plan(K, M, GV_ROWS, stages, sslots)) mode = GV_ROWS;
-    else if (!gv_plan(K, M, GV_KSPLIT, stages, sslots)) return cudaErrorInvalidValue;
+    // row-split (two CTAs per SM where they fit) when its units fill the
+    // GPU; else k-split, one CTA per SM with all of its shared memory (two
+    // per SM measured no faster for single calls)
+    if (units_r >= sms && (gv_plan(K, MT, GV_ROWS, true, stages, sslots) ||
+                           gv_plan(K, MT, GV_ROWS, false, stages, sslots)))
+        mode = GV_ROWS;
+    else if (!gv_plan(K, MT, GV_KSPLIT, false, stages, sslots))
+        return cudaErrorInvalidValue;
 
     GemvTab<NJ> tab;
     tab.njobs = G;
     tab.K = K;
+    tab.M = M;
     int64_t units = 0;
     for (int g = 0; g < G; ++g) {
         const tq2_weight* w = ws[g];
@@ -587,11 +661,16 @@ cudaError_t gv_dispatch(const tq2_weight* const* ws, const float* const* xs, flo
         tab.job[g].unit0 = (int)units;
         units += (w->N + gv_unit_rows(mode) - 1) / gv_unit_rows(mode);
     }
-    if (M == 1)
-        return mode == GV_ROWS ? gv_launch<1, GV_ROWS>(tab, (int)units, stages, sslots, sms, dev, st)
-                               : gv_launch<1, GV_KSPLIT>(tab, (int)units, stages, sslots, sms, dev, st);
-    return mode == GV_ROWS ? gv_launch<2, GV_ROWS>(tab, (int)units, stages, sslots, sms, dev, st)
-                           : gv_launch<2, GV_KSPLIT>(tab, (int)units, stages, sslots, sms, dev, st);
+#define GV_LAUNCH(T)                                                                     \
+    return mode == GV_ROWS ? gv_launch<T, GV_ROWS>(tab, (int)units, stages, sslots, sms, dev, st) \
+                           : gv_launch<T, GV_KSPLIT>(tab, (int)units, stages, sslots, sms, dev, st)
+    switch (MT) {
+        case 1: GV_LAUNCH(1);
+        case 2: GV_LAUNCH(2);
+        case 4: GV_LAUNCH(4);
+        default: GV_LAUNCH(8);
+    }
+#undef GV_LAUNCH
 }
 
 bool make_map(tq2_weight* w, CUtensorMap* map, uint32_t rows, uint32_t pieces) {
@@ -606,7 +685,7 @@ bool make_map(tq2_weight* w, CUtensorMap* map, uint32_t rows, uint32_t pieces) {
 }  // namespace
 
 bool gemv_supports(int M, int64_t K) {
-    return M >= 1 && M <= GEMV_MAX_M && K >= 128 && (int64_t)M * K <= GEMV_MAX_MK;
+    return M >= 1 && M <= GEMV_MAX_M && K >= 128 && (int64_t)gv_mt(M) * K <= GEMV_MAX_MK;
 }
 
 bool make_gemv_maps(tq2_weight* w) {

@@ -65,10 +65,11 @@ cudaError_t launch_skinny(const uint8_t* codes, const uint16_t* scales, const fl
                           int N, int K, void* scratch, cudaStream_t st);
 unsigned int read_clear_dev_error_skinny(cudaStream_t st);
 
-// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M and M*K <= GEMV_MAX_MK (no
+// tq2_gemv.cu: fused GEMV for M <= GEMV_MAX_M and MT*K <= GEMV_MAX_MK, MT = M
+// rounded up to 1, 2, 4 or 8 (no
 // scratch; x lives in shared memory); one launch runs G <= GEMV_MAX_JOBS
 // independent GEMVs of the same K and M.
-constexpr int GEMV_MAX_M = 2;
+constexpr int GEMV_MAX_M = 8;
 constexpr int64_t GEMV_MAX_MK = 32768;
 constexpr int GEMV_MAX_JOBS = 64;
 bool gemv_supports(int M, int64_t K);
@@ -81,7 +82,8 @@ unsigned int read_clear_dev_error_gemv(cudaStream_t st);
 bool make_umma_maps(tq2_weight* w);
 size_t tensor_scratch_bytes(int64_t M, int64_t K);
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
-                          cudaStream_t st);
+                          cudaStream_t st, int bn_force = 0,
+                          int splits_force = 0);
 unsigned int read_clear_dev_error_umma(cudaStream_t st);
 
 // blr_rank.cu: res = oscale * f16(act . vec * scale) P over the sign plane of

@@ -320,9 +320,10 @@ unsigned int read_clear_dev_error_skinny(cudaStream_t st) {
 // plugin or custom-op interface that forbids allocation inside its enqueue
 // call, a serving process that reserved all device memory up front, or a
 // real-time loop where an allocator call could stall or fail.  For them,
-// tq2_gemm_skinny_static keeps its scratch (the staged hi/lo f16 fragments
-// of x) in the fixed device array below instead of asking the stream-ordered
-// allocator, and calls no allocating routine at all.
+// tq2_gemm_skinny_static runs the fused GEMV where it applies (it has no
+// scratch) and otherwise keeps the staged kernel's scratch (the hi/lo f16
+// fragments of x) in the fixed device array below instead of asking the
+// stream-ordered allocator; it calls no allocating routine at all.
 // --------------------------------------------------------------------------
 namespace {
 
@@ -370,26 +371,34 @@ extern "C" TQ2_API tq2_status tq2_gemm_skinny_static(tq2_handle h, const float* 
                                      (long long)N, (long long)K, (long long)h->N, (long long)h->K);
     if ((reinterpret_cast<uintptr_t>(x) & 15) != 0)
         return (tq2_status)tq2::set_error(TQ2_EINVAL, "tq2_gemm_skinny_static: x must be 16-byte aligned");
-    const size_t need = tq2::skinny_scratch_bytes(M, K);
-    if (need > kStaticScratchBytes)
-        return (tq2_status)tq2::set_error(TQ2_ESHAPE,
-                                     "tq2_gemm_skinny_static: needs %zu bytes of scratch for M=%lld K=%lld, above the "
-                                     "fixed %zu-byte area (ceil(M/4)*K*16 must be <= %zu)",
-                                     need, (long long)M, (long long)K, kStaticScratchBytes, kStaticScratchBytes);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
         return (tq2_status)tq2::set_error(TQ2_EINVAL,
                                           "tq2_gemm_skinny_static: the handle lives on device %d but device %d is "
                                           "current (the fixed scratch array is per device)",
                                           h->device, dev);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Shapes the fused GEMV takes need no scratch at all: the same kernel as
+    // tq2_gemm, so the results are the same bit for bit.
+    if (tq2::gemv_supports((int)M, K)) {
+        cudaError_t e = tq2::launch_gemv(&h, &x, &out, 1, (int)M, st);
+        if (e != cudaSuccess)
+            return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: gemv launch: %s", cudaGetErrorString(e));
+        return TQ2_OK;
+    }
+    const size_t need = tq2::skinny_scratch_bytes(M, K);
+    if (need > kStaticScratchBytes)
+        return (tq2_status)tq2::set_error(TQ2_ESHAPE,
+                                     "tq2_gemm_skinny_static: needs %zu bytes of scratch for M=%lld K=%lld, above the "
+                                     "fixed %zu-byte area (ceil(M/4)*K*16 must be <= %zu)",
+                                     need, (long long)M, (long long)K, kStaticScratchBytes, kStaticScratchBytes);
     void* scratch = nullptr;
     cudaError_t e = static_scratch(&scratch);
     if (e != cudaSuccess)
         return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
     // Every element of the scratch that the GEMM reads is written first by the
     // staging kernel of the same call, so nothing needs clearing.
-    e = tq2::launch_skinny(h->codes, h->scales, x, out, (int)M, (int)N, (int)K, scratch,
-                      reinterpret_cast<cudaStream_t>(stream));
+    e = tq2::launch_skinny(h->codes, h->scales, x, out, (int)M, (int)N, (int)K, scratch, st);
     if (e != cudaSuccess)
         return (tq2_status)tq2::set_error(TQ2_ECUDA, "tq2_gemm_skinny_static: launch: %s", cudaGetErrorString(e));
     return TQ2_OK;

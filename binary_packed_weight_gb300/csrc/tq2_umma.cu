@@ -58,9 +58,9 @@ bool make_umma_maps(tq2_weight* w) {
 }
 
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
-                          cudaStream_t st) {
+                          cudaStream_t st, int bn_force, int splits_force) {
     const int N = (int)w->N, K = (int)w->K;
-    const int BN = umma_pick_bn(M);
+    const int BN = bn_force > 0 ? bn_force : umma_pick_bn(M);
     const int tiles_n = (N + UM_BM - 1) / UM_BM;
     const int tiles_m = (M + BN - 1) / BN;
     const int nk = K / UM_BK;
@@ -73,7 +73,7 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
     const int cl = (BN > 128 && tiles_n >= 2) ? 2 : 1;
     const int slots = sms / cl, units1 = ((tiles_n + cl - 1) / cl) * tiles_m;
     auto longest = [&](int sp) { return ((units1 * sp + slots - 1) / slots) * ((nk + sp - 1) / sp); };
-    const int splits = (nk >= 4 && longest(2) < longest(1)) ? 2 : 1;
+    const int splits = splits_force > 0 ? splits_force : ((nk >= 4 && longest(2) < longest(1)) ? 2 : 1);
 
     uint32_t* xh = reinterpret_cast<uint32_t*>(scratch);
     const int64_t groups = (int64_t)M * (K / 16);

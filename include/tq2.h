@@ -147,8 +147,9 @@ TQ2_API tq2_status tq2_shape(tq2_handle h, int64_t* N, int64_t* K);
  * terms, hi = f16(x) and lo = f16(x - hi), whose sum differs from x by at
  * most about 2^-22 |x| (the weights are exact), with f32 accumulation:
  * |error| <= 2^-12 sum_k |x[m,k] W[n,k]| + 1e-7 per element, which is within
- * the pages' 1e-3 at K <= 4096 for unit-scale data.  For M <= 2 and
- * M*K <= 32768 it is a single kernel with no scratch; that kernel decodes
+ * the pages' 1e-3 at K <= 4096 for unit-scale data.  For M <= 8 and
+ * MT*K <= 32768, with MT = M rounded up to 1, 2, 4 or 8, it is a single
+ * kernel with no scratch (the fused GEMV); that kernel decodes
  * codes with an offset that it removes per 128-block, so the rounding of a
  * block that holds a nonzero weight scales with that block's sum of |x|
  * (tested within the bound above on weights with 99 % zeros and x up to 256x
@@ -167,9 +168,26 @@ TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64
                          int path, void* stream);
 
 /*
+ * tq2_gemm_tensor_tuned -- the tensor-core path of tq2_gemm with its tile
+ * shape chosen by the caller (tuning sweeps; no counterpart on the pages).
+ *
+ *   bn      tokens per tile: 0 = the library's choice, else a multiple of 16
+ *           in 16..256; one that is not a multiple of 32 must be >= M.
+ *   splits  K splits: 0 = the library's choice, else 1..8 and <= K/64.  With
+ *           more than one split the partial sums are added into the
+ *           (zeroed) output with atomic adds: two splits give the same bits
+ *           in either order, more than two may differ between runs by
+ *           rounding (all within the tensor-path bound of tq2_gemm).
+ *   Other arguments and errors as tq2_gemm on its tensor path; a bad bn or
+ *   splits returns TQ2_EINVAL.
+ */
+TQ2_API tq2_status tq2_gemm_tensor_tuned(tq2_handle h, const float* x, float* out, int64_t M, int64_t N,
+                                         int64_t K, int bn, int splits, void* stream);
+
+/*
  * tq2_gemm_grouped -- G independent decode-shape GEMMs in one launch:
  * out_g[m,n] = sum_k x_g[m,k] * W_g[n,k] for g < G, each as tq2_gemm with
- * M <= 2 computes it (same kernel, same per-output arithmetic, so results
+ * M <= 8 computes it (same kernel, same per-output arithmetic, so results
  * are bit-identical to G separate tq2_gemm calls).  One launch streams all
  * G weights, so independent projections that read the same activations
  * (or different ones) do not pay G kernel launches and G dependency waits.
@@ -177,8 +195,9 @@ TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64
  *   hs      HOST array of G handles; all must have the same K.
  *   xs      HOST array of G DEVICE pointers, float[M][K] each, 16-byte aligned.
  *   outs    HOST array of G DEVICE pointers, float[M][N_g] each (overwritten).
- *   G       1..64;  M in {1, 2} with M*K <= 32768 (x is held in shared
- *           memory);  K the handles' K.  Else TQ2_ESHAPE.
+ *   G       1..64;  1 <= M <= 8 with MT*K <= 32768, MT = M rounded up to
+ *           1, 2, 4 or 8 (x is held in shared memory);  K the handles' K.
+ *           Else TQ2_ESHAPE.
  *   stream  asynchronous; no scratch is allocated.
  */
 TQ2_API tq2_status tq2_gemm_grouped(const tq2_handle* hs, const float* const* xs, float* const* outs, int G,
@@ -228,14 +247,14 @@ TQ2_API tq2_status tq2_quantize(const float* w, int64_t N, int64_t K, void* aos_
  * processes that reserve all device memory up front, and real-time loops in
  * which an allocator call could stall or fail.
  *
- *   Same arguments as tq2_gemm with 1 <= M <= 16; it always runs the staged
- *   skinny kernel, so its results equal tq2_gemm's bit for bit for M >= 3 and
- *   differ from them only by rounding for M <= 2, where tq2_gemm takes the
- *   fused GEMV (both within the skinny bound of tq2_gemm).
+ *   Same arguments as tq2_gemm with 1 <= M <= 16; it runs the same kernel
+ *   as tq2_gemm (the fused GEMV where that applies, which needs no scratch,
+ *   else the staged skinny kernel), so its results equal tq2_gemm's bit for
+ *   bit.
  *   The handle must live on the current device, else TQ2_EINVAL.
- *   Scratch: a fixed 1 MiB device array inside the library (one per GPU that
- *   loads it, held until the process exits) holds the staged f16 fragments
- *   of x, ceil(M/4)*K*16 bytes; larger requests (for example K > 16384 at
+ *   Scratch (staged kernel only): a fixed 1 MiB device array inside the
+ *   library (one per GPU that loads it, held until the process exits) holds
+ *   the staged f16 fragments of x, ceil(M/4)*K*16 bytes; larger requests (for example K > 16384 at
  *   M = 16, K > 65536 at M <= 4) return TQ2_ESHAPE.  No cudaMalloc,
  *   cudaFree or stream-ordered allocation is made.
  *   The first call on a device looks up the array's device address on the

@@ -38,6 +38,7 @@ def test_tq2_calls(lib):
     for M in (-1, (1 << 24) + 1):                                      # refused before the handle is read
         assert lib.tq2_gemm(A, A, A, M, 16, 128, None) == TQ2_ESHAPE, M
     assert lib.tq2_gemm_path(None, A, A, 1, 16, 128, 1, None) == TQ2_EINVAL
+    assert lib.tq2_gemm_tensor_tuned(None, A, A, 32, 16, 128, 32, 1, None) == TQ2_EINVAL
     assert lib.tq2_gemm_skinny_static(None, A, A, 1, 16, 128, None) == TQ2_EINVAL
     assert lib.tq2_shape(None, None, None) == TQ2_EINVAL
     assert lib.tq2_unpack(None, A, None) == TQ2_EINVAL
@@ -47,8 +48,10 @@ def test_tq2_calls(lib):
     assert lib.tq2_gemm_grouped(hs, hs, hs, 0, 1, 128, None) == TQ2_ESHAPE
     assert lib.tq2_gemm_grouped(hs, hs, hs, 65, 1, 128, None) == TQ2_ESHAPE
     assert "G <= 64" in _err(lib)
-    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 3, 128, None) == TQ2_ESHAPE   # M <= 2 only
-    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 2, 32768, None) == TQ2_ESHAPE  # M*K <= 32768
+    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 9, 128, None) == TQ2_ESHAPE   # M <= 8 only
+    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 2, 32768, None) == TQ2_ESHAPE  # MT*K <= 32768
+    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 3, 16384, None) == TQ2_ESHAPE  # M = 3 counts as MT = 4
+    assert lib.tq2_gemm_grouped(hs, hs, hs, 1, 5, 8192, None) == TQ2_ESHAPE   # M = 5 counts as MT = 8
 
 
 def test_debug_wait_timeout_bound(lib):

@@ -75,12 +75,14 @@ def test_skinny_page_sweep(lib, N, K):
         check_skinny(got, ref, absref, f"sweep N={N} K={K} M={M}")
 
 
-def test_gemv_two_tokens_full_size(lib):
+def test_gemv_tokens_full_size(lib):
+    """The fused GEMV at the decode-shape weight for every token count it
+    takes (M = 3 and 5..7 padded to four and eight tokens)."""
     cfg = synth.GEMV
     N, K = cfg["N"], cfg["K"]
     aos = synth.random_tq2(N, K, cfg["wkey"])
     w = lib.tq2_upload(aos, N, K)
-    for M in (2, 3):
+    for M in (2, 3, 4, 5, 6, 7, 8):
         x = synth.random_x(M, K, cfg["xkey"] + M)
         got = run_gemm(lib, w, x)
         ref, absref, _, _ = oracle_gemm(aos, N, K, x)
@@ -88,16 +90,16 @@ def test_gemv_two_tokens_full_size(lib):
 
 
 def test_gemv_large_k_chunks(lib):
-    # K = 16384: each warp walks several 4-block chunks
-    N, K = 300, 16384
-    aos = synth.random_tq2(N, K, 90)
-    w = lib.tq2_upload(aos, N, K)
-    for M in (1, 2):
-        x = synth.random_x(M, K, 91) * 0.5
-        got = run_gemm(lib, w, x)
-        ref, absref, _, _ = oracle_gemm(aos, N, K, x)
-        assert np.max(np.abs(got - ref)) <= 2e-3, np.max(np.abs(got - ref))
-        assert np.all(np.abs(got - ref) <= (2.0 ** -10) * absref + 1e-7)
+    # K = 16384 (M <= 2) and 8192 (M <= 4): each warp walks several 4-block chunks
+    for N, K, Ms in ((300, 16384, (1, 2)), (300, 8192, (3, 4))):
+        aos = synth.random_tq2(N, K, 90)
+        w = lib.tq2_upload(aos, N, K)
+        for M in Ms:
+            x = synth.random_x(M, K, 91) * 0.5
+            got = run_gemm(lib, w, x)
+            ref, absref, _, _ = oracle_gemm(aos, N, K, x)
+            assert np.max(np.abs(got - ref)) <= 2e-3, (M, np.max(np.abs(got - ref)))
+            assert np.all(np.abs(got - ref) <= (2.0 ** -10) * absref + 1e-7), M
 
 
 def test_gemv_grouped_matches_single_calls(lib):
@@ -109,7 +111,7 @@ def test_gemv_grouped_matches_single_calls(lib):
         a = synth.random_tq2(N, K, key)
         auos.append(a)
         ws.append(lib.tq2_upload(a, N, K))
-    for M in (1, 2):
+    for M in (1, 2, 3, 8):
         xs = [to_dev(synth.random_x(M, K, 50 + g)) for g in range(len(ws))]
         outs = [torch.full((M, w.N), float("nan"), device="cuda") for w in ws]
         lib.tq2_gemm_grouped(ws, xs, outs)
@@ -121,9 +123,9 @@ def test_gemv_grouped_matches_single_calls(lib):
             assert torch.equal(outs[g], single), (M, g)
             ref, absref, _, _ = oracle_gemm(auos[g], w.N, K, xs[g].cpu().numpy())
             check_skinny(outs[g].cpu().numpy().astype(np.float64), ref, absref, f"grouped M={M} g={g}")
-    with pytest.raises(lib.TQ2Error):                       # M = 3 is not a grouped shape
-        x3 = [torch.zeros((3, K), device="cuda") for _ in ws]
-        lib.tq2_gemm_grouped(ws, x3, [torch.zeros((3, w.N), device="cuda") for w in ws])
+    with pytest.raises(lib.TQ2Error):                       # M = 9 is not a grouped shape
+        x9 = [torch.zeros((9, K), device="cuda") for _ in ws]
+        lib.tq2_gemm_grouped(ws, x9, [torch.zeros((9, w.N), device="cuda") for w in ws])
 
 
 def test_gemv_many_units_per_cta_sampled(lib):
@@ -137,7 +139,7 @@ def test_gemv_many_units_per_cta_sampled(lib):
     codes, d_bits = otq2.parse_aos(aos, N, K)
     rng = np.random.Generator(np.random.Philox(key=93))
     rows = sorted(set(rng.integers(0, N, 600).tolist()) | set(range(20)) | set(range(N - 20, N)))
-    for M in (1, 2):
+    for M in (1, 2, 4, 8):
         x = synth.random_x(M, K, 94 + M)
         xd = to_dev(x)
         out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
@@ -194,12 +196,12 @@ def _sampled_gemv_check(lib, N, K, Ms, wkey, xkey, nsample=400):
 def test_gemv_row_split_ragged(lib):
     """Row-split GEMV with a ragged last unit (20000 = 156 x 128 + 32 rows)
     and a partial last stage (K = 2176: 17 blocks)."""
-    _sampled_gemv_check(lib, 20000, 2176, (1, 2), 110, 111)
+    _sampled_gemv_check(lib, 20000, 2176, (1, 2, 5), 110, 111)
 
 
 def test_gemv_row_split_k8192(lib):
-    """Row-split GEMV at K = 8192, M = 1 and 2 (x held in shared memory)."""
-    _sampled_gemv_check(lib, 19600, 8192, (1, 2), 112, 113, nsample=200)
+    """Row-split GEMV at K = 8192, M = 1..4 (x held in shared memory)."""
+    _sampled_gemv_check(lib, 19600, 8192, (1, 2, 3, 4), 112, 113, nsample=200)
 
 
 def test_gemv_grouped_distinct_x(lib):
@@ -211,7 +213,7 @@ def test_gemv_grouped_distinct_x(lib):
     aoss = [synth.random_tq2(N, K, 120 + i) for i in range(3)]
     ws = [lib.tq2_upload(a, N, K) for a in aoss]
     Ws = [otq2.dequant_aos(a, N, K) for a in aoss]
-    for M in (1, 2):
+    for M in (1, 2, 6):
         xs_np = [synth.random_x(M, K, 300 + 10 * M + g) for g in range(G)]
         hs = [ws[g % 3] for g in range(G)]
         outs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(G)]
@@ -225,13 +227,14 @@ def test_gemv_grouped_distinct_x(lib):
 
 
 def test_gemv_mk_limit(lib):
-    """M * K above the shared-memory limit of the fused GEMV: a single call
-    falls back to the staged skinny kernel, a grouped call is refused."""
+    """MT * K above the shared-memory limit of the fused GEMV (MT = M rounded
+    up to 1, 2, 4, 8): a single call falls back to the staged skinny kernel,
+    a grouped call is refused."""
     import torch
     N, K = 40, 16512                     # M = 2: M * K = 33024 > 32768
     aos = synth.random_tq2(N, K, 95)
     w = lib.tq2_upload(aos, N, K)
-    for M in (1, 2):
+    for M in (1, 2, 3, 5, 8):
         x = synth.random_x(M, K, 96) * 0.5
         got = run_gemm(lib, w, x)
         ref, absref, _, _ = oracle_gemm(aos, N, K, x)
@@ -314,6 +317,38 @@ def test_tensor_skinny_config_full(lib, M):
     x = synth.random_x(M, K, cfg["xkey"])
     got = run_gemm(lib, w, x)
     check_tensor(got, *oracle_gemm(aos, N, K, x), where=f"N=11008 M={M}")
+
+
+def test_tensor_tuned_tiles_and_splits(lib):
+    """The tensor path under every token tile and K-split count the tuning
+    export accepts for these shapes (ragged row tile, ragged token tile, K
+    of 10 k-steps so that three splits are uneven): each within the tensor
+    bound against the oracle, two splits bit-equal to one another run to run;
+    bad tiles and split counts are refused."""
+    import torch
+    N, K = 300, 640
+    aos = synth.random_tq2(N, K, 130)
+    w = lib.tq2_upload(aos, N, K)
+    for M, tiles in ((33, (48, 64, 128)), (100, (32, 64, 128, 256))):
+        x = synth.random_x(M, K, 131 + M)
+        ref, absref, ref16, absref16 = oracle_gemm(aos, N, K, x)
+        xd = to_dev(x)
+        for bn in tiles:
+            for splits in (1, 2, 3, 4):
+                out = torch.full((M, N), float("nan"), device="cuda")
+                lib.tq2_gemm_tensor_tuned(w, xd, out, bn, splits)
+                lib.device_status()
+                got = out.cpu().numpy().astype(np.float64)
+                check_tensor(got, ref, absref, ref16, absref16, f"tuned M={M} bn={bn} splits={splits}")
+                if splits <= 2:
+                    again = torch.full((M, N), float("nan"), device="cuda")
+                    lib.tq2_gemm_tensor_tuned(w, xd, again, bn, splits)
+                    assert torch.equal(out, again), (M, bn, splits)
+    x = to_dev(synth.random_x(60, K, 140))
+    out = torch.zeros((60, N), device="cuda")
+    for bn, splits in ((48, 1), (8, 1), (272, 1), (64, 11), (64, 9)):   # 48 < M = 60 is not a multiple of 32
+        with pytest.raises(lib.TQ2Error):
+            lib.tq2_gemm_tensor_tuned(w, x, out, bn, splits)
 
 
 def test_tensor_large_sampled(lib):
@@ -508,7 +543,7 @@ def _sparse_weights(N, K, key, p_nonzero, zero_rows=()):
 @pytest.mark.parametrize("p_nonzero", [0.1, 0.01])
 @pytest.mark.parametrize("xscale", [1.0, 16.0, 256.0])
 def test_gemv_sparse_weights_scaled_x(lib, p_nonzero, xscale):
-    """M = 1 and 2 through tq2_gemm (the fused GEMV) and tq2_gemm_grouped on
+    """M = 1, 2, 4, 8 through tq2_gemm (the fused GEMV) and tq2_gemm_grouped on
     weights with >= 90 % zero codes, rows of all code 1 mixed with dense rows,
     and x ~ N(0,1) times 1, 16 and 256: element by element within
     2^-12 * sum|x W| + 1e-7 (f32 accumulation), and exactly 0 on the all-zero
@@ -520,7 +555,7 @@ def test_gemv_sparse_weights_scaled_x(lib, p_nonzero, xscale):
         aos, codes = _sparse_weights(N, K, 700 + int(1000 * p_nonzero), p_nonzero, zr)
         w = lib.tq2_upload(aos, N, K)
         W = otq2.dequant_aos(aos, N, K)
-        for M in (1, 2):
+        for M in ((1, 2, 4, 8) if K <= 4096 else (1, 2, 4)):
             x = (synth.random_x(M, K, 710 + M) * np.float32(xscale)).astype(np.float32)
             ref, absref = otq2.gemm(x, W), otq2.gemm_abs(x, W)
             got = run_gemm(lib, w, x)

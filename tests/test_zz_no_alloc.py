@@ -4,10 +4,12 @@ Callers that must not allocate device memory during a GEMM (plugin or
 custom-op interfaces that forbid allocation while enqueuing work, serving
 processes that reserve all device memory up front, real-time loops) use
 tq2_gemm_skinny_static, whose scratch is a fixed device array inside the
-library.  This test calls it through the C ABI twice in a row per shape and
-checks each result against the f64 oracle within the skinny kernel's bound,
-and, for M >= 3 where tq2_gemm runs the same staged skinny kernel, for bit
-equality with tq2_gemm.  The file name makes pytest collect it last.
+library (the fused GEMV, where it applies, needs none).  This test calls it
+through the C ABI twice in a row per shape and checks each result against
+the f64 oracle within the skinny kernel's bound and for bit equality with
+tq2_gemm, which runs the same kernel: the fused GEMV for M <= 8 at this K,
+the staged skinny kernel above that.  The file name makes pytest collect it
+last.
 """
 import ctypes
 
@@ -39,15 +41,14 @@ def test_static_scratch_matches_oracle_and_regular_entry_point(lib):
     aos = synth.random_tq2(N, K, 301)
     w = lib.tq2_upload(aos, N, K)
     W = otq2.dequant_aos(aos, N, K)
-    for M in (1, 2, 3, 6, 16):
+    for M in (1, 2, 3, 6, 9, 16):
         x = synth.random_x(M, K, 302 + M)
         ref, absref = otq2.gemm(x, W), otq2.gemm_abs(x, W)
         regular = _run(lib, "tq2_gemm", w, x)
         for call in range(2):                               # two calls in a row
             got = _run(lib, "tq2_gemm_skinny_static", w, x)
             check_skinny(got, ref, absref, f"static M={M} call {call}")
-            if M >= 3:                                      # the same kernel as tq2_gemm
-                assert np.array_equal(got, regular), M
+            assert np.array_equal(got, regular), M          # the same kernel as tq2_gemm
 
 
 def test_static_scratch_refuses_oversized_requests(lib):
