@@ -60,20 +60,35 @@ bool make_umma_maps(tq2_weight* w) {
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,
                           cudaStream_t st, int bn_force, int splits_force) {
     const int N = (int)w->N, K = (int)w->K;
-    const int BN = bn_force > 0 ? bn_force : umma_pick_bn(M);
     const int tiles_n = (N + UM_BM - 1) / UM_BM;
-    const int tiles_m = (M + BN - 1) / BN;
     const int nk = K / UM_BK;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // The wide 384-token tile (a decoded stage feeds 1.5x the tokens, A in
+    // tensor memory) when the CTA pairs' rounds of tiles make it cheaper than
+    // 256 tokens a tile: per token it runs ~7 % faster (measured at M=1536,
+    // N=27648, K=3072), but its coarser tiles can leave a last round
+    // half-empty (at M=4096, N=14336 it needs 9 rounds for 8.1 rounds of
+    // work against 12 for 11.8).
+    int BN = umma_pick_bn(M);
+    if (M >= UM_WIDE_BN && tiles_n >= 2) {
+        const int pairs = sms / 2, np = (tiles_n + 1) / 2;
+        const long long rounds_w = (np * ((M + UM_WIDE_BN - 1) / UM_WIDE_BN) + pairs - 1) / pairs;
+        const long long rounds_n = (np * ((M + UM_MAX_BN - 1) / UM_MAX_BN) + pairs - 1) / pairs;
+        if (rounds_w * UM_WIDE_BN * 93 < rounds_n * UM_MAX_BN * 100) BN = UM_WIDE_BN;
+    }
+    if (bn_force > 0) BN = bn_force;
+    const int tiles_m = (M + BN - 1) / BN;
     // K splits: 1 or 2 (two partials add into a zeroed output in either
     // order to the same sum); two only when they shorten the longest walk of
-    // a CTA (or CTA pair) over its units of work
+    // a CTA (or CTA pair) over its units of work by a quarter or more: the
+    // atomic epilogue reads and writes the output twice (at M=4096 x
+    // N=14336 a 6 % shorter walk cost 28 % more time)
     const int cl = (BN > 128 && tiles_n >= 2) ? 2 : 1;
     const int slots = sms / cl, units1 = ((tiles_n + cl - 1) / cl) * tiles_m;
     auto longest = [&](int sp) { return ((units1 * sp + slots - 1) / slots) * ((nk + sp - 1) / sp); };
-    const int splits = splits_force > 0 ? splits_force : ((nk >= 4 && longest(2) < longest(1)) ? 2 : 1);
+    const int splits = splits_force > 0 ? splits_force : ((nk >= 4 && 4 * longest(2) <= 3 * longest(1)) ? 2 : 1);
 
     uint32_t* xh = reinterpret_cast<uint32_t*>(scratch);
     const int64_t groups = (int64_t)M * (K / 16);

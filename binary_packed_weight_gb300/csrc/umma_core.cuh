@@ -37,6 +37,10 @@ constexpr int UM_BK = 64;        // K per pipeline stage (128 bytes of f16)
 constexpr int UM_STAGES = 8;     // B / A ring slots allocated; the launch picks how many it uses
 constexpr int UM_RAW_STAGES = 32;   // raw plane ring slots allocated
 constexpr int UM_MAX_BN = 256;   // MMA N limit for M = 128
+// The wide token tile: one 384-column accumulator and a 4-stage A ring in
+// tensor memory fill its 512 columns, so a decoded stage feeds 384 tokens
+// (two MMAs per k-step, N = 256 and 128) without a shared-memory A ring.
+constexpr int UM_WIDE_BN = 384;
 constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in shared memory (16 KB)
 // warp 0 activation TMA, warp 1 MMA, warp 2 TMEM allocator, warp 3 plane TMA,
 // warps 4-11 decoders (two per 32-row quarter of the tile, taking alternate stages),
@@ -321,7 +325,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // barrier is tested without blocking before this stage's MMAs are
         // issued, so a stage that is already complete costs no wait at all.
         // Every MMA and commit is issued by one lane chosen with elect.sync.
-        const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)BN);
+        const uint32_t idesc = idesc_f16_f32(UM_BM, (uint32_t)(BN > UM_MAX_BN ? UM_MAX_BN : BN));
+        const uint32_t idesc2 = idesc_f16_f32(UM_BM, (uint32_t)(BN > UM_MAX_BN ? BN - UM_MAX_BN : 16));
         int lt = 0, s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -353,10 +358,22 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
                 if (AT) {
                     const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (UM_BK / 2));
+                    if (BN > UM_MAX_BN) {
+                        // tokens 256.. of the tile: rows 256.. of the B stage (1 KB swizzle atoms)
+                        const uint64_t bdesc2 = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes + UM_MAX_BN * 128));
 #pragma unroll
-                    for (int j = 0; j < UM_BK / 16; ++j)
-                        umma_f16_ts_elect(dcol, acol + (uint32_t)(j * 8), bdesc + (uint64_t)(2 * j), idesc,
-                                          (kc > k0 || j > 0) ? 1u : 0u);
+                        for (int j = 0; j < UM_BK / 16; ++j) {
+                            const uint32_t acc = (kc > k0 || j > 0) ? 1u : 0u;
+                            umma_f16_ts_elect(dcol, acol + (uint32_t)(j * 8), bdesc + (uint64_t)(2 * j), idesc, acc);
+                            umma_f16_ts_elect(dcol + (uint32_t)UM_MAX_BN, acol + (uint32_t)(j * 8),
+                                              bdesc2 + (uint64_t)(2 * j), idesc2, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < UM_BK / 16; ++j)
+                            umma_f16_ts_elect(dcol, acol + (uint32_t)(j * 8), bdesc + (uint64_t)(2 * j), idesc,
+                                              (kc > k0 || j > 0) ? 1u : 0u);
+                    }
                 } else {
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(a_ring + s * UM_A_STAGE));
 #pragma unroll
@@ -520,26 +537,31 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 template <class Dec, int MODE, bool AT>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
-    if (BN > UM_MAX_BN || BN % 16 != 0 || BN < 16 || (AT && BN > 128)) return cudaErrorInvalidValue;
+    const bool wide = BN == UM_WIDE_BN;
+    if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide) || (wide && !AT))
+        return cudaErrorInvalidValue;
     // the epilogue drains 32 columns at a time: a tile narrower than a
     // multiple of 32 must be the only token tile
     if (BN % 32 != 0 && T > BN) return cudaErrorInvalidValue;
     const int tiles_n = (R + UM_BM - 1) / UM_BM;
-    const int cl = (!AT && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
+    const int cl = ((!AT || wide) && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
+    if (BN / cl > 256) return cudaErrorInvalidValue;      // a TMA box is at most 256 rows
     CUtensorMap xmap;
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
                             (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // two accumulators in tensor memory (the epilogue of a tile overlaps the
-    // next tile's MMAs); the B ring (and the A ring unless AT) in shared
-    // memory, then the raw plane ring with what is left; with AT the A ring
-    // takes S x 32 tensor-memory columns after the accumulators
-    // (2 x 128 + 8 x 32 = 512 at most)
-    const int NACC = 2;
+    // next tile's MMAs), one for the wide tile (its epilogue, ~3 % of a
+    // tile's K loop, stalls the MMAs); the B ring (and the A ring unless AT)
+    // in shared memory, then the raw plane ring with what is left; with AT
+    // the A ring takes S x 32 tensor-memory columns after the accumulators
+    // (2 x 128 + 8 x 32 or 384 + 4 x 32 = 512 at most)
+    const int NACC = wide ? 1 : 2;
     const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024;
     const int a_stage = AT ? 0 : UM_A_STAGE;
     const int raw = Dec::DIRECT ? 0 : Dec::RAW;
     int S = UM_STAGES;
+    if (AT && S > (512 - NACC * BN) / (UM_BK / 2)) S = (512 - NACC * BN) / (UM_BK / 2);   // A ring in tensor memory
     // leave room for at least 8 raw stages
     while (S > 2 && (size_t)S * (BN * 128 + a_stage) + (size_t)8 * raw > budget) --S;
     int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (BN * 128 + a_stage)) / (size_t)(raw > 0 ? raw : 1));
@@ -593,7 +615,8 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
 template <class Dec, int MODE>
 cudaError_t launch_umma(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                         int splits, cudaStream_t st) {
-    if (BN <= 128 && !Dec::DIRECT) return launch_umma_impl<Dec, MODE, true>(pm, ep, act16, T, R, K, BN, splits, st);
+    if ((BN <= 128 || BN == UM_WIDE_BN) && !Dec::DIRECT)
+        return launch_umma_impl<Dec, MODE, true>(pm, ep, act16, T, R, K, BN, splits, st);
     return launch_umma_impl<Dec, MODE, false>(pm, ep, act16, T, R, K, BN, splits, st);
 }
 

@@ -323,13 +323,15 @@ def test_tensor_tuned_tiles_and_splits(lib):
     """The tensor path under every token tile and K-split count the tuning
     export accepts for these shapes (ragged row tile, ragged token tile, K
     of 10 k-steps so that three splits are uneven): each within the tensor
-    bound against the oracle, two splits bit-equal to one another run to run;
-    bad tiles and split counts are refused."""
+    bound against the oracle, two splits bit-equal to one another run to run
+    (the 384-token tile included: partial at M = 100, two tiles at M = 600, an
+    odd number of 128-row tiles for its CTA pairs); bad tiles and split counts
+    are refused."""
     import torch
     N, K = 300, 640
     aos = synth.random_tq2(N, K, 130)
     w = lib.tq2_upload(aos, N, K)
-    for M, tiles in ((33, (48, 64, 128)), (100, (32, 64, 128, 256))):
+    for M, tiles in ((33, (48, 64, 128)), (100, (32, 64, 128, 256, 384)), (600, (384,))):
         x = synth.random_x(M, K, 131 + M)
         ref, absref, ref16, absref16 = oracle_gemm(aos, N, K, x)
         xd = to_dev(x)
