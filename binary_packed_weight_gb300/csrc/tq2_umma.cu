@@ -85,7 +85,7 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
     // a CTA (or CTA pair) over its units of work by a quarter or more: the
     // atomic epilogue reads and writes the output twice (at M=4096 x
     // N=14336 a 6 % shorter walk cost 28 % more time)
-    const int cl = (BN > 128 && tiles_n >= 2) ? 2 : 1;
+    const int cl = (BN > UM_MAX_BN && tiles_n >= 2) ? 2 : 1;
     const int slots = sms / cl, units1 = ((tiles_n + cl - 1) / cl) * tiles_m;
     auto longest = [&](int sp) { return ((units1 * sp + slots - 1) / slots) * ((nk + sp - 1) / sp); };
     const int splits = splits_force > 0 ? splits_force : ((nk >= 4 && 4 * longest(2) <= 3 * longest(1)) ? 2 : 1);

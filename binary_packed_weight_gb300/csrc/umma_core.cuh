@@ -16,11 +16,12 @@
 //   * eight decoder warps (one plane row per thread, two warps per 32-row
 //     quarter taking alternate stages) expand a raw stage from shared memory
 //     into the f16 A operand: into tensor memory when the token tile is at
-//     most 128 wide (AT), otherwise into a shared-memory ring in the MMA's
-//     K-major 128-byte-swizzled layout;
+//     most 128 wide or the 384-token wide tile (AT), otherwise into a
+//     shared-memory ring in the MMA's K-major 128-byte-swizzled layout;
 //   * one warp issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
-//     one of two accumulators and frees stages with tcgen05.commit; every
-//     MMA is issued by one lane of the converged warp (elect.sync);
+//     one of two accumulators (one for the wide tile) and frees stages with
+//     tcgen05.commit; every MMA is issued by one lane of the converged warp
+//     (elect.sync);
 //   * four epilogue warps read the finished accumulator (tcgen05.ld), hand it
 //     back, and run the epilogue policy of the call while the next tile's
 //     MMAs proceed in the other accumulator.
@@ -531,9 +532,12 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 // Host: launch one GEMM.  act16 is f16 [T][K] (row pitch K), staged in the
 // decoder's K order; R = plane rows; splits = K splits; pm = the plane's
 // tensor maps.  Token tiles of at most 128 keep the decoded weights in
-// tensor memory (AT) and run without clusters; wider tiles decode into shared
-// memory and pair CTAs on neighbouring weight tiles to share the activation
-// tile.  Dense planes always take the shared-memory path (TMA writes A).
+// tensor memory (AT), and so does the 384-token wide tile; 256-token tiles
+// decode into shared memory.  Dense planes always take the shared-memory path
+// (TMA writes A).  Only the wide tile pairs CTAs on neighbouring weight tiles
+// to share its activation tile (192 rows each by multicast: a TMA box is at
+// most 256 rows); pairing at 256 tokens measured slower (a multicast tile
+// lands at about half the rate of one a CTA loads alone).
 template <class Dec, int MODE, bool AT>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
@@ -544,7 +548,7 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     // multiple of 32 must be the only token tile
     if (BN % 32 != 0 && T > BN) return cudaErrorInvalidValue;
     const int tiles_n = (R + UM_BM - 1) / UM_BM;
-    const int cl = ((!AT || wide) && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
+    const int cl = (wide && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
     if (BN / cl > 256) return cudaErrorInvalidValue;      // a TMA box is at most 256 rows
     CUtensorMap xmap;
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
