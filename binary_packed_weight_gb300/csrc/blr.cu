@@ -162,15 +162,25 @@ __global__ void colsum_prod_kernel(const float* __restrict__ A, const float* __r
     }
 }
 
-// out[n] += sum_c colpart[c][n], c in order.
-__global__ void colsum_finish_kernel(const float* __restrict__ colpart, int chunks, int n, float* __restrict__ out) {
+// The backward's three column sums in one launch: job blockIdx.y of
+// {dh, dl, dg}, out[n] += sum_c colpart[c][n], c in order (the same order and
+// arithmetic for each of the three).
+struct ColsumJobs {
+    const float* colpart[3];
+    int chunks[3], n[3];
+    float* out[3];
+};
+__global__ void colsum_finish3_kernel(const ColsumJobs jobs) {
     pdl_wait();
     pdl_launch_dependents();
+    const int q = blockIdx.y;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n) return;
+    if (j >= jobs.n[q]) return;
+    const float* cp = jobs.colpart[q];
+    const int n = jobs.n[q];
     float s = 0.f;
-    for (int c = 0; c < chunks; ++c) s += colpart[(int64_t)c * n + j];
-    out[j] += s;
+    for (int c = 0; c < jobs.chunks[q]; ++c) s += cp[(int64_t)c * n + j];
+    jobs.out[q][j] += s;
 }
 
 unsigned int read_clear_dev_error_blr(cudaStream_t st) {
@@ -215,11 +225,6 @@ cudaError_t stage32(const float* src, const float* col, float scale, void* dst, 
     if (blocks > cap) blocks = cap;
     return launch_pdl(stage32_kernel, dim3((unsigned)blocks), dim3(256), 0, st, src, col, scale,
                       reinterpret_cast<uint32_t*>(dst), (int64_t)T, (int64_t)Kd);
-}
-
-cudaError_t colsum_finish(const float* colpart, int chunks, int n, float* out, cudaStream_t st) {
-    return launch_pdl(colsum_finish_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, colpart, chunks, n,
-                      out);
 }
 
 }  // namespace
@@ -300,44 +305,51 @@ tq2_status backward_one(const char* who, const uint32_t* bits_u, const uint32_t*
     const int iT = (int)T, din = (int)d_in, dout = (int)d_out, ir = (int)r;
     const int BN = blr_bn(iT);
     const int ttiles = (iT + BN - 1) / BN, chunks = (iT + FIN_TC - 1) / FIN_TC;
-    const int64_t mx = d_in > d_out ? d_in : d_out;
-    const size_t bytes = (size_t)T * r * 2 + 256 + (size_t)(ttiles > chunks ? ttiles : chunks) * (mx + r) * 4 + 1024;
+    // column-sum partials of dh, dl and dg each in their own buffer, so that one
+    // launch at the end finishes all three
+    const int dh_parts = c_save ? chunks : ttiles;
+    const size_t bytes = (size_t)T * r * 2 + 256 + ((size_t)dh_parts * d_out + 256) * 4 +
+                         ((size_t)chunks * r + 256) * 4 + ((size_t)ttiles * d_in + 256) * 4 + 1024;
     void* mem = nullptr;
     cudaError_t e = cudaMallocAsync(&mem, bytes, st);
     if (e != cudaSuccess) return cuda_status(e, who);
     Scratch sc{reinterpret_cast<char*>(mem), 0};
     uint16_t* r16 = sc.take<uint16_t>((size_t)T * r);         // a.l (dh recompute), then b.l.gs
-    float* colp = sc.take<float>((size_t)(ttiles > chunks ? ttiles : chunks) * mx);
+    float* colp_h = sc.take<float>((size_t)dh_parts * d_out);
+    float* colp_l = sc.take<float>((size_t)chunks * r);
+    float* colp_g = sc.take<float>((size_t)ttiles * d_in);
     const float inv_gs = 1.0f / gscale;
 
     // dh += sum_t dy.c
     if (c_save) {
         e = launch_pdl(colsum_prod_kernel, dim3((unsigned)((dout + 31) / 32), (unsigned)chunks), dim3(32, 8), 0, st,
-                       dy, c_save, iT, dout, colp);
-        if (e == cudaSuccess) e = colsum_finish(colp, chunks, dout, dh, st);
+                       dy, c_save, iT, dout, colp_h);
     } else {                                                 // recompute c = (a.l) S_U^T in the GEMM
         e = stage32(a_save, l, 1.0f, r16, iT, ir, st);
         if (e == cudaSuccess) {
             PlaneMaps pm;
-            EpiArgs ep{nullptr, nullptr, nullptr, dy, colp, (int64_t)d_out, 1.0f};
+            EpiArgs ep{nullptr, nullptr, nullptr, dy, colp_h, (int64_t)d_out, 1.0f};
             e = plane_maps_sign(pm, bits_u, dout, ir)
                     ? launch_umma<DecSign, EPI_COLSUM>(pm, ep, r16, iT, dout, ir, BN, 1, st)
                     : cudaErrorInvalidValue;
         }
-        if (e == cudaSuccess) e = colsum_finish(colp, ttiles, dout, dh, st);
     }
     // b = (dy.h.gs) S_U / gs in one pass over dy; dl += sum_t a.b; stage f16(b.l.gs)
     if (e == cudaSuccess)
-        e = launch_blr_rank(dy, h, gscale, bits_u, iT, dout, ir, inv_gs, nullptr, l, gscale, r16, a_save, colp, st);
-    if (e == cudaSuccess) e = colsum_finish(colp, chunks, ir, dl, st);
+        e = launch_blr_rank(dy, h, gscale, bits_u, iT, dout, ir, inv_gs, nullptr, l, gscale, r16, a_save, colp_l, st);
     // dx' = (b.l.gs) S_V / gs; dx = g.dx'; dg += sum_t x.dx'
     if (e == cudaSuccess) {
         PlaneMaps pm;
-        EpiArgs ep{dx, nullptr, g, x, colp, (int64_t)d_in, inv_gs, accumulate};
+        EpiArgs ep{dx, nullptr, g, x, colp_g, (int64_t)d_in, inv_gs, accumulate};
         e = plane_maps_sign(pm, bits_v, din, ir)
                 ? launch_umma<DecSign, EPI_SCALE_COLSUM>(pm, ep, r16, iT, din, ir, BN, 1, st)
                 : cudaErrorInvalidValue;
-        if (e == cudaSuccess) e = colsum_finish(colp, ttiles, din, dg, st);
+    }
+    // dh, dl, dg += their column sums, one launch
+    if (e == cudaSuccess) {
+        ColsumJobs jobs{{colp_h, colp_l, colp_g}, {dh_parts, chunks, ttiles}, {dout, ir, din}, {dh, dl, dg}};
+        const int mxn = din > dout ? (din > ir ? din : ir) : (dout > ir ? dout : ir);
+        e = launch_pdl(colsum_finish3_kernel, dim3((unsigned)((mxn + 255) / 256), 3u), dim3(256), 0, st, jobs);
     }
     cudaError_t e2 = cudaFreeAsync(mem, st);
     if (e != cudaSuccess) return cuda_status(e, who);
