@@ -292,21 +292,23 @@ def extra_skinny(torch, bpw, stream, dev, pk, Ms):
 
 def extra_c3_sweep(torch, bpw, stream, dev, pk):
     """Token-tile x K-split sweep of the tensor path at the batched-decode
-    shapes M = 32 and 128, N = 11008, K = 4096 (24 weight copies, > L2):
+    shapes M = 8, 32 and 128, N = 11008, K = 4096 (24 weight copies, > L2):
     microseconds per GEMM (x staging included) for every tile and split
-    count, plus the library's own choice (bn 0, splits 0)."""
+    count, plus the library's own choice for the tensor path (bn 0, splits
+    0; at M = 8 tq2_gemm itself takes the fused GEMV).  The weight-row tile
+    is fixed at 128 rows, the M of a one-CTA kind::f16 MMA."""
     cfg = synth.SKINNY
     N, K = cfg["N"], cfg["K"]
     aos = synth.random_tq2(N, K, cfg["wkey"])
     copies = 24
     ws = [bpw.tq2_upload(aos, N, K) for _ in range(copies)]
     res = {}
-    for M, tiles in ((32, (0, 32)), (128, (0, 32, 64, 128))):
+    for M, tiles in ((8, (0, 16)), (32, (0, 32)), (128, (0, 32, 64, 128))):
         x = torch.from_numpy(synth.random_x(M, K, cfg["xkey"])).to(dev)
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
         row = {}
         for bn in tiles:
-            for splits in ((0,) if bn == 0 else (1, 2, 4, 8)):
+            for splits in ((0,) if bn == 0 else (1, 2, 4, 8, 16)):
                 def step():
                     for w in ws:
                         bpw.tq2_gemm_tensor_tuned(w, x, out, bn, splits, stream=stream.cuda_stream)

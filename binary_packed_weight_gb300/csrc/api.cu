@@ -244,12 +244,12 @@ tq2_status tq2_gemm_tensor_tuned(tq2_handle h, const float* x, float* out, int64
     if ((reinterpret_cast<uintptr_t>(x) & 15) != 0)
         return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: x must be 16-byte aligned");
     // token tile: a multiple of 16 up to 256 (one that is not a multiple of
-    // 32 must cover all M tokens), or 384 with N > 128; K splits: 1..8 and
-    // at most K/64
+    // 32 must cover all M tokens), or 384 with N > 128; K splits: 1..16
+    // and at most K/64
     const bool wide = bn == 384 && N > 128;
     if (bn != 0 && !wide && (bn < 16 || bn > 256 || bn % 16 != 0 || (bn % 32 != 0 && M > bn)))
         return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: bad token tile %d", bn);
-    if (splits != 0 && (splits < 1 || splits > 8 || splits > K / 64))
+    if (splits != 0 && (splits < 1 || splits > 16 || splits > K / 64))
         return fail(TQ2_EINVAL, "tq2_gemm_tensor_tuned: bad split count %d", splits);
     cudaStream_t st = S(stream);
     void* scratch = nullptr;

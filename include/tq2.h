@@ -174,7 +174,7 @@ TQ2_API tq2_status tq2_gemm_path(tq2_handle h, const float* x, float* out, int64
  *   bn      tokens per tile: 0 = the library's choice, else a multiple of 16
  *           in 16..256 (one that is not a multiple of 32 must be >= M), or
  *           384 when N > 128.
- *   splits  K splits: 0 = the library's choice, else 1..8 and <= K/64.  With
+ *   splits  K splits: 0 = the library's choice, else 1..16 and <= K/64.  With
  *           more than one split the partial sums are added into the
  *           (zeroed) output with atomic adds: two splits give the same bits
  *           in either order, more than two may differ between runs by

@@ -348,7 +348,7 @@ def test_tensor_tuned_tiles_and_splits(lib):
                     assert torch.equal(out, again), (M, bn, splits)
     x = to_dev(synth.random_x(60, K, 140))
     out = torch.zeros((60, N), device="cuda")
-    for bn, splits in ((48, 1), (8, 1), (272, 1), (64, 11), (64, 9)):   # 48 < M = 60 is not a multiple of 32
+    for bn, splits in ((48, 1), (8, 1), (272, 1), (64, 11), (64, 17)):   # 48 < M = 60 is not a multiple of 32
         with pytest.raises(lib.TQ2Error):
             lib.tq2_gemm_tensor_tuned(w, x, out, bn, splits)
 
