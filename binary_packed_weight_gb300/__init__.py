@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load", "lib_path", "TQ2Error", "Weight", "tq2_upload", "tq2_gemm", "tq2_gemm_path", "tq2_gemm_tensor_tuned",
-    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths", "blr_sign_grads",
+    "tq2_gemm_skinny_static", "tq2_gemm_grouped", "GroupedGemv", "tq2_unpack", "tq2_dequant_f16", "tq2_quantize", "blr_expand_bits", "blr_forward", "blr_backward", "blr_forward_paths", "blr_backward_paths", "blr_sign_grads",
     "device_status", "debug_wait_timeout", "PATH_AUTO", "PATH_SKINNY", "PATH_TENSOR",
 ]
 
@@ -166,6 +166,25 @@ def tq2_gemm_grouped(ws, xs, outs, stream=None):
     _check(load().tq2_gemm_grouped(ctypes.cast(hs, _P), ctypes.cast(xp, _P), ctypes.cast(op, _P), G, M, K,
                                    _stream(stream)), "tq2_gemm_grouped")
     return outs
+
+
+class GroupedGemv:
+    """tq2_gemm_grouped with its arguments marshalled once: the handle and
+    pointer arrays are built at construction (the tensors are kept alive), so a
+    loop that calls the same group every step pays one C call per step."""
+
+    def __init__(self, ws, xs, outs):
+        self._keep = (list(ws), list(xs), list(outs))
+        self.G = len(ws)
+        self.M, self.K = xs[0].shape
+        self._hs = (_P * self.G)(*[w.handle for w in ws])
+        self._xp = (_P * self.G)(*[x.data_ptr() for x in xs])
+        self._op = (_P * self.G)(*[o.data_ptr() for o in outs])
+        self._args = (ctypes.cast(self._hs, _P), ctypes.cast(self._xp, _P), ctypes.cast(self._op, _P))
+
+    def __call__(self, stream=None):
+        _check(load().tq2_gemm_grouped(*self._args, self.G, self.M, self.K, _stream(stream)), "tq2_gemm_grouped")
+        return self._keep[2]
 
 
 def tq2_unpack(w, stream=None):

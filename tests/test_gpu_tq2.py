@@ -116,6 +116,14 @@ def test_gemv_grouped_matches_single_calls(lib):
         outs = [torch.full((M, w.N), float("nan"), device="cuda") for w in ws]
         lib.tq2_gemm_grouped(ws, xs, outs)
         lib.device_status()
+        # the same group with its arguments marshalled once, called twice
+        outs2 = [torch.full((M, w.N), float("nan"), device="cuda") for w in ws]
+        grp = lib.GroupedGemv(ws, xs, outs2)
+        for _ in range(2):
+            grp()
+            lib.device_status()
+            for g in range(len(ws)):
+                assert torch.equal(outs2[g], outs[g]), (M, g)
         for g, w in enumerate(ws):
             single = torch.empty_like(outs[g])
             lib.tq2_gemm(w, xs[g], single)
