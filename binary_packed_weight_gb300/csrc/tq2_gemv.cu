@@ -38,9 +38,10 @@
 //         keeps eight partial sums that mirror the k-split warps, so both
 //         ways give bit-identical results.
 // Row-split launches keep shared memory under ~110 KB so that two CTAs share
-// an SM; k-split launches give their one CTA per SM all of it (a deeper
-// ring).  The next kernel on the stream is launched early (programmatic
-// dependent launch) and takes SM room as this grid's CTAs leave.
+// an SM; k-split launches run one CTA on every SM, under ~110 KB where x
+// leaves room for four stages, so the next kernel on the stream (launched
+// early through programmatic dependent launch) fits beside it and streams
+// its own weights.
 #include "ptx.cuh"
 #include "tq2_internal.h"
 
@@ -575,12 +576,14 @@ __global__ void __maxnreg__(gv_maxnreg(MT, MODE))
 namespace {
 
 // Ring depth and scale slots: with `pair`, as many stages as fit beside a
-// second CTA of the grid (false below four); else all of an SM's shared
-// memory, which also keeps the next kernel's CTAs (launched early) off the SM
-// until this grid's CTA leaves -- early CTAs that doubled up on SMs a
-// one-per-SM grid left idle made chained GEMVs slower.  Enough scale slots
-// that the code ring, not the scales, limits how far the producer runs
-// ahead.  False if nothing fits.
+// second CTA (false below four), else all of an SM's shared memory.
+// Row-split grids put two of their own CTAs on an SM; k-split grids put one
+// CTA on every SM and take the pair budget when it leaves four stages, so
+// the next kernel's CTA (launched early) fits beside it on every SM and
+// streams its weights meanwhile (chained 4096^2 GEMVs 4.9 -> 4.8 us; with a
+// grid that left SMs idle the early CTAs doubled up there and ran slower).
+// Enough scale slots that the code ring, not the scales, limits how far the
+// producer runs ahead.  False if nothing fits.
 bool gv_plan(int K, int MT, int mode, bool pair, int& stages, int& sslots) {
     sslots = 2;
     for (int pass = 0; pass < 2; ++pass) {
@@ -638,12 +641,12 @@ cudaError_t gv_dispatch(const tq2_weight* const* ws, const float* const* xs, flo
     int stages = 0, sslots = 0;
     int mode = GV_KSPLIT;
     // row-split (two CTAs per SM where they fit) when its units fill the
-    // GPU; else k-split, one CTA per SM with all of its shared memory (two
-    // per SM measured no faster for single calls)
+    // GPU; else k-split, one CTA per SM (two per SM measured no faster for
+    // single calls), within the pair budget when four stages fit there
     if (units_r >= sms && (gv_plan(K, MT, GV_ROWS, true, stages, sslots) ||
                            gv_plan(K, MT, GV_ROWS, false, stages, sslots)))
         mode = GV_ROWS;
-    else if (!gv_plan(K, MT, GV_KSPLIT, false, stages, sslots))
+    else if (!gv_plan(K, MT, GV_KSPLIT, true, stages, sslots) && !gv_plan(K, MT, GV_KSPLIT, false, stages, sslots))
         return cudaErrorInvalidValue;
 
     GemvTab<NJ> tab;
