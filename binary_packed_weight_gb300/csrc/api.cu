@@ -139,10 +139,16 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     if (e == cudaSuccess) e = cudaMalloc(&w->scales, (size_t)nblocks * 2 + 16);
     if (e == cudaSuccess) e = cudaMemset(w->scales + nblocks, 0, 16);
     if (e == cudaSuccess) e = cudaMalloc(&w->scales_t, (size_t)(K / 128) * w->Np * 2);
-    if (e != cudaSuccess) {
+    if (e == cudaSuccess) e = cudaMalloc(&w->codes_t, (size_t)(K / 4) * w->Np);
+    auto release = [w]() {
         cudaFree(w->codes);
         cudaFree(w->scales);
+        cudaFree(w->scales_t);
+        cudaFree(w->codes_t);
         delete w;
+    };
+    if (e != cudaSuccess) {
+        release();
         return cuda_fail(e, "tq2_upload: cudaMalloc");
     }
     uint8_t* tmp = nullptr;
@@ -150,20 +156,15 @@ tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, vo
     if (e == cudaSuccess) e = cudaMemcpyAsync(tmp, aos, aos_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = tq2::launch_repack(tmp, w->codes, w->scales, nblocks, st);
     if (e == cudaSuccess) e = tq2::launch_scales_t(w->scales, w->scales_t, N, K / 128, w->Np, st);
+    if (e == cudaSuccess) e = tq2::launch_codes_t(w->codes, w->codes_t, N, K, w->Np, st);
     if (tmp) cudaFreeAsync(tmp, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
-        cudaFree(w->codes);
-        cudaFree(w->scales);
-        cudaFree(w->scales_t);
-        delete w;
+        release();
         return cuda_fail(e, "tq2_upload");
     }
     if (!tq2::make_gemv_maps(w) || !tq2::make_umma_maps(w)) {
-        cudaFree(w->codes);
-        cudaFree(w->scales);
-        cudaFree(w->scales_t);
-        delete w;
+        release();
         return fail(TQ2_EUNSUPPORTED, "tq2_upload: cuTensorMapEncodeTiled refused a code-plane map");
     }
     *out = w;
@@ -175,7 +176,9 @@ tq2_status tq2_free(tq2_handle h) {
     cudaError_t e1 = cudaFree(h->codes);
     cudaError_t e2 = cudaFree(h->scales);
     cudaError_t e3 = cudaFree(h->scales_t);
+    cudaError_t e4 = cudaFree(h->codes_t);
     delete h;
+    if (e4 != cudaSuccess) return cuda_fail(e4, "tq2_free");
     if (e3 != cudaSuccess) return cuda_fail(e3, "tq2_free");
     if (e1 != cudaSuccess) return cuda_fail(e1, "tq2_free");
     if (e2 != cudaSuccess) return cuda_fail(e2, "tq2_free");

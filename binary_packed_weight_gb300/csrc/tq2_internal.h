@@ -20,12 +20,14 @@ struct tq2_weight {
     uint8_t* codes = nullptr;      // [N][K/4], then 128 bytes of padding
     uint16_t* scales = nullptr;    // [N][K/128] f16 bits, then 16 bytes of padding
     uint16_t* scales_t = nullptr;  // [K/128][Np] the same bits block-major (rows >= N zero), for the tensor path
+    uint8_t* codes_t = nullptr;    // [Np/128][K/64][128 rows][16 B] the same codes stage-tiled (rows >= N zero),
+                                   // for the tensor path: one K-stage of a 128-row tile is 2 KB contiguous
     int device = 0;
     // 3D views of the code plane for the GEMV's TMA loads, built at upload:
     // (128-byte piece, row, piece index), strides (1, K/4, 128) bytes; boxes
     // of 16 rows x 8 pieces (k-split units) and 128 rows x 1 piece (row units).
     CUtensorMap gemv_map_k, gemv_map_r;
-    // the tensor path's views: code tiles of 128 rows x 16 bytes and
+    // the tensor path's views: 2 KB code stages of the stage-tiled copy and
     // block-major scale rows of 128 (umma_core.cuh, plane_maps_tq2)
     tq2::PlaneMaps umma_maps;
 };
@@ -58,6 +60,7 @@ cudaError_t launch_unpack(const uint8_t* codes, const uint16_t* scales, uint8_t*
                           cudaStream_t st);
 cudaError_t launch_scales_t(const uint16_t* scales, uint16_t* scales_t, int64_t N, int64_t nb, int64_t Np,
                             cudaStream_t st);
+cudaError_t launch_codes_t(const uint8_t* codes, uint8_t* codes_t, int64_t N, int64_t K, int64_t Np, cudaStream_t st);
 cudaError_t launch_dequant_f16(const uint8_t* codes, const uint16_t* scales, uint16_t* w, int64_t N,
                                int64_t K, cudaStream_t st);
 size_t skinny_scratch_bytes(int64_t M, int64_t K);

@@ -63,6 +63,19 @@ __global__ void scales_t_kernel(const uint16_t* __restrict__ scales, uint16_t* _
     scales_t[i] = n < N ? scales[n * nb + b] : (uint16_t)0;
 }
 
+// Stage-tiled copy of the code plane for the tensor path: the 16 bytes (64
+// codes) of row n in K-stage kc go to codes_t[n/128][kc][n%128], rows
+// N <= n < Np zero.  One thread per 16-byte chunk, reading along a row.
+__global__ void codes_t_kernel(const uint8_t* __restrict__ codes, uint8_t* __restrict__ codes_t, int64_t N,
+                               int64_t nkc, int64_t Np) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= Np * nkc) return;
+    const int64_t n = i / nkc, kc = i % nkc;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) v = *reinterpret_cast<const uint4*>(codes + (n * nkc + kc) * 16);
+    *reinterpret_cast<uint4*>(codes_t + (((n >> 7) * nkc + kc) * 128 + (n & 127)) * 16) = v;
+}
+
 // W as f16 bits, natural order, through the same pair decode the GEMMs use:
 // one thread per 32-bit code word (16 elements).
 __global__ void dequant_f16_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
@@ -259,6 +272,13 @@ cudaError_t launch_scales_t(const uint16_t* scales, uint16_t* scales_t, int64_t 
                             cudaStream_t st) {
     const int64_t n = nb * Np;
     scales_t_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(scales, scales_t, N, nb, Np);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_codes_t(const uint8_t* codes, uint8_t* codes_t, int64_t N, int64_t K, int64_t Np,
+                           cudaStream_t st) {
+    const int64_t n = Np * (K / 64);
+    codes_t_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(codes, codes_t, N, K / 64, Np);
     return cudaGetLastError();
 }
 

@@ -54,7 +54,7 @@ __global__ void stage_x_f16_kernel(const float* __restrict__ x, uint32_t* __rest
 size_t tensor_scratch_bytes(int64_t M, int64_t K) { return (size_t)(M * K * 2); }
 
 bool make_umma_maps(tq2_weight* w) {
-    return plane_maps_tq2(w->umma_maps, w->codes, w->scales_t, (int)w->N, (int)w->K, (int)w->Np);
+    return plane_maps_tq2(w->umma_maps, w->codes_t, w->scales_t, (int)w->K, (int)w->Np);
 }
 
 cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M, void* scratch,

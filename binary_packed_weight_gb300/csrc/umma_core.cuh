@@ -72,13 +72,16 @@ struct UmmaBars {
 // of a word at bits 2e; pair q = (element q, element q+8); the block scale is
 // folded in: (c-1)*d is exact in f16.  Activations staged in 16-element
 // groups.  Raw stage: codes [128 rows][16 B], then the stage's block scales
-// [128 rows] (from the block-major copy of the scale plane made at upload).
+// [128 rows], both from the copies made at upload for this path (the codes
+// stage-tiled, so a stage is 2 KB contiguous and lands as 16 lines of 128
+// bytes; the scales block-major).  A 16-byte-wide box of the row-major plane
+// streams at only about one row per 5 cycles.
 struct DecTQ2 {
     static constexpr int RAW = UM_BM * 16 + UM_BM * 2;
     static constexpr bool DIRECT = false;
     __device__ __forceinline__ static void issue(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* raw,
                                                  uint64_t* bar, int row0, int kc) {
-        tma_load_2d(raw, m0, bar, kc * 16, row0);              // codes: x in bytes
+        tma_load_3d(raw, m0, bar, 0, kc * 16, row0 >> 7);     // codes: 16 lines of 128 B
         tma_load_2d(raw + UM_BM * 16, m1, bar, row0, kc / 2);   // scales: x = row, y = block
     }
     __device__ __forceinline__ static void decode(const uint8_t* raw, int r, int kc, uint32_t (&v)[32]) {
@@ -143,10 +146,14 @@ struct DecDense {
 
 // Host side: the tensor maps a plane's decoder loads from (PlaneMaps,
 // tq2_internal.h).
-// TQ2: codes [R][K/4] bytes; block-major scales [K/128][Rp] (Rp a multiple of 128)
-inline bool plane_maps_tq2(PlaneMaps& pm, const uint8_t* codes, const uint16_t* scales_t, int R, int K, int Rp) {
-    return make_tensor_map_2d(&pm.m0, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(codes), (uint64_t)K / 4,
-                              (uint64_t)R, (uint64_t)K / 4, 16u, (uint32_t)UM_BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+// TQ2: stage-tiled codes [Rp/128][K/64][128][16 B] viewed as (128-byte line,
+// line of the tile, tile); block-major scales [K/128][Rp] (Rp a multiple of 128)
+inline bool plane_maps_tq2(PlaneMaps& pm, const uint8_t* codes_t, const uint16_t* scales_t, int K, int Rp) {
+    const uint64_t dims[3] = {128u, (uint64_t)K / 4, (uint64_t)Rp / UM_BM};
+    const uint64_t strides[2] = {128u, (uint64_t)K / 4 * 128u};
+    const uint32_t box[3] = {128u, 16u, 1u};
+    return make_tensor_map_3d(&pm.m0, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(codes_t), dims, strides,
+                              box, CU_TENSOR_MAP_SWIZZLE_NONE) &&
            make_tensor_map_2d(&pm.m1, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<uint16_t*>(scales_t), (uint64_t)Rp,
                               (uint64_t)K / 128, (uint64_t)Rp * 2, (uint32_t)UM_BM, 1u, CU_TENSOR_MAP_SWIZZLE_NONE);
 }

@@ -116,8 +116,12 @@ TQ2_API tq2_status tq2_debug_wait_timeout(uint64_t limit_ns, void* stream);
  *
  * Device layout behind the handle ("SoA"): a code plane uint8[N][K/4]
  * holding each row's qs bytes in K order, and a scale plane uint16[N][K/128]
- * of f16 bits, each followed by a little zeroed padding.  Codes are not
- * validated: code 3 decodes as +2 (3-1).
+ * of f16 bits, each followed by a little zeroed padding.  The tensor-core
+ * path (M > 8) reads two further copies made here: the codes stage-tiled
+ * (uint8[ceil(N/128)][K/64][128][16], a 64-code stage of 128 rows
+ * contiguous) and the scales block-major (uint16[K/128][ceil(N/128)*128]),
+ * rows past N zero; so a handle holds about 2*N*K/4 + N*K/64 bytes.  Codes
+ * are not validated: code 3 decodes as +2 (3-1).
  */
 TQ2_API tq2_status tq2_upload(const void* aos, int64_t N, int64_t K, tq2_handle* out, void* stream);
 
