@@ -420,8 +420,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         }
                         uint32_t v[32];
                         Dec::decode(raw_ring + r * Dec::RAW, arow, kc, v);
-                        // the raw slot is refilled through the async proxy
-                        fence_proxy_async_shared();
+                        // no proxy fence before releasing the slot: its reads
+                        // are ordered before the (release) arrive, and the TMA
+                        // that refills it is issued after the producer's wait
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
                         if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
