@@ -84,9 +84,26 @@ struct DecTQ2 {
         tma_load_3d(raw, m0, bar, 0, kc * 16, row0 >> 7);     // codes: 16 lines of 128 B
         tma_load_2d(raw + UM_BM * 16, m1, bar, row0, kc / 2);   // scales: x = row, y = block
     }
+    // a 128-k stage (one block): codes [2][128 rows][16 B], then the block's scales
+    static constexpr int RAW2 = UM_BM * 32 + UM_BM * 2;
+    __device__ __forceinline__ static void issue2(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* raw,
+                                                  uint64_t* bar, int row0, int kb) {
+        tma_load_3d(raw, m0, bar, 0, kb * 32, row0 >> 7);
+        tma_load_3d(raw + UM_BM * 16, m0, bar, 0, kb * 32 + 16, row0 >> 7);
+        tma_load_2d(raw + UM_BM * 32, m1, bar, row0, kb);
+    }
+    // half hf (k 64*hf .. 64*hf+63) of row r of a 128-k stage
+    __device__ __forceinline__ static void decode2(const uint8_t* raw, int r, int kb, int hf, uint32_t (&v)[32]) {
+        expand(*reinterpret_cast<const uint4*>(raw + hf * (UM_BM * 16) + r * 16),
+               reinterpret_cast<const uint16_t*>(raw + UM_BM * 32)[r], v);
+        (void)kb;
+    }
     __device__ __forceinline__ static void decode(const uint8_t* raw, int r, int kc, uint32_t (&v)[32]) {
-        const uint4 c = *reinterpret_cast<const uint4*>(raw + r * 16);
-        const uint16_t d = reinterpret_cast<const uint16_t*>(raw + UM_BM * 16)[r];
+        expand(*reinterpret_cast<const uint4*>(raw + r * 16), reinterpret_cast<const uint16_t*>(raw + UM_BM * 16)[r],
+               v);
+        (void)kc;
+    }
+    __device__ __forceinline__ static void expand(const uint4 c, const uint16_t d, uint32_t (&v)[32]) {
         const __half2 d2 = __halves2half2(__ushort_as_half(d), __ushort_as_half(d));
         const uint32_t words[4] = {c.x, c.y, c.z, c.w};
         uint32_t p[8];
@@ -99,7 +116,6 @@ struct DecTQ2 {
                 v[w * 8 + q] = *reinterpret_cast<uint32_t*>(&hh);
             }
         }
-        (void)kc;
     }
 };
 
@@ -130,6 +146,16 @@ struct DecSign {
         word(w.x, v);
         word(w.y, v + 16);
     }
+    // a 128-k stage: the same four words a row
+    static constexpr int RAW2 = UM_BM * 16;
+    __device__ __forceinline__ static void issue2(const CUtensorMap* m0, const CUtensorMap*, uint8_t* raw,
+                                                  uint64_t* bar, int row0, int kb) {
+        tma_load_2d(raw, m0, bar, kb * 4, row0);
+    }
+    __device__ __forceinline__ static void decode2(const uint8_t* raw, int r, int kb, int hf, uint32_t (&v)[32]) {
+        decode(raw, r, hf, v);
+        (void)kb;
+    }
 };
 
 // Dense f16 rows, already in the K order the activations are staged in
@@ -142,6 +168,10 @@ struct DecDense {
         tma_load_2d(a_stage, m0, bar, kc * UM_BK, row0);
     }
     __device__ __forceinline__ static void decode(const uint8_t*, int, int, uint32_t (&)[32]) {}
+    static constexpr int RAW2 = 0;   // no 128-k stages (the shared-memory A path only)
+    __device__ __forceinline__ static void issue2(const CUtensorMap*, const CUtensorMap*, uint8_t*, uint64_t*, int,
+                                                  int) {}
+    __device__ __forceinline__ static void decode2(const uint8_t*, int, int, int, uint32_t (&)[32]) {}
 };
 
 // Host side: the tensor maps a plane's decoder loads from (PlaneMaps,
@@ -217,17 +247,23 @@ struct TileMap {
 // columns a stage after the NACC accumulators) instead of shared memory, and
 // the MMAs read A from there; for token tiles of at most 128, where the
 // shared-memory round trip of the decoded rows would cost more than the MMAs.
-template <class Dec, int MODE, bool AT>
+// K2 (with AT): a pipeline stage spans 128 k (two 64-k swizzle atoms of
+// activations, 64 tensor-memory columns of A, eight MMAs), which halves the
+// per-stage waits, commits and hand-offs that set the pace of narrow token
+// tiles; the MMA sequence, and so the result, is that of two 64-k stages.
+template <class Dec, int MODE, bool AT, bool K2 = false>
 __global__ void __launch_bounds__(UM_THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap0,
                  const __grid_constant__ CUtensorMap amap1, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
                  const TileMap tm, int S, int SR, int NACC, int cl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int stage_bytes = BN * 128;
+    constexpr int KA = K2 ? 2 : 1;                       // 64-k atoms a stage
+    constexpr int RAWB = K2 ? Dec::RAW2 : Dec::RAW;      // raw plane bytes a stage
+    const int stage_bytes = BN * 128 * KA;               // [KA][BN rows][128 B]
     uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned (!AT)
-    uint8_t* raw_ring = a_ring + (AT ? 0 : S * UM_A_STAGE);          // [SR][Dec::RAW] (!DIRECT)
-    UmmaBars* bars = reinterpret_cast<UmmaBars*>(raw_ring + (Dec::DIRECT ? 0 : SR * Dec::RAW));
+    uint8_t* raw_ring = a_ring + (AT ? 0 : S * UM_A_STAGE);          // [SR][RAWB] (!DIRECT)
+    UmmaBars* bars = reinterpret_cast<UmmaBars*>(raw_ring + (Dec::DIRECT ? 0 : SR * RAWB));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
     // tiles of the same unit and share its activation tile: each loads 1/cl
@@ -265,6 +301,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const uint32_t a_col0 = (uint32_t)(NACC * BN);       // first column of the A ring (AT)
+    constexpr uint32_t A_COLS = (uint32_t)(UM_BK / 2 * KA);   // tensor-memory columns of an A stage
     volatile int* abort_flag = &bars->abort;
 
     pdl_launch_dependents();
@@ -291,8 +328,12 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                     if (cl > 1)
                         tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full[s], kc * UM_BK,
                                        m * BN + rank * part, cmask);
-                    else
-                        tma_load_2d(smem + s * stage_bytes, &xmap, &bars->full[s], kc * UM_BK, m * BN);
+                    else {
+#pragma unroll
+                        for (int a = 0; a < KA; ++a)
+                            tma_load_2d(smem + s * stage_bytes + a * BN * 128, &xmap, &bars->full[s],
+                                        (kc * KA + a) * UM_BK, m * BN);
+                    }
                     if (Dec::DIRECT) Dec::issue(&amap0, &amap1, a_ring + s * UM_A_STAGE, &bars->full[s], row0, kc);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
@@ -317,8 +358,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->raw_full[r], (uint32_t)Dec::RAW);
-                    Dec::issue(&amap0, &amap1, raw_ring + r * Dec::RAW, &bars->raw_full[r], row0, kc);
+                    mbar_arrive_expect_tx(&bars->raw_full[r], (uint32_t)RAWB);
+                    if (K2) Dec::issue2(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
+                    else Dec::issue(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
                     if (++r == SR) { r = 0; ph ^= 1u; }
                 }
             }
@@ -364,7 +406,18 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 ready = mbar_test_wait(&bars->full[s1], ph1);   // its latency hides under the MMAs below
                 tc_fence_after();
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
-                if (AT) {
+                if (AT && K2) {
+                    // atom a of the B stage at a * BN rows; k-step j of atom a at A column (4a + j) * 8
+                    const uint32_t acol = tmem + a_col0 + (uint32_t)s * A_COLS;
+#pragma unroll
+                    for (int a = 0; a < KA; ++a) {
+                        const uint64_t bda = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes + a * BN * 128));
+#pragma unroll
+                        for (int j = 0; j < UM_BK / 16; ++j)
+                            umma_f16_ts_elect(dcol, acol + (uint32_t)((a * (UM_BK / 16) + j) * 8),
+                                              bda + (uint64_t)(2 * j), idesc, (kc > k0 || a > 0 || j > 0) ? 1u : 0u);
+                    }
+                } else if (AT) {
                     const uint32_t acol = tmem + a_col0 + (uint32_t)(s * (UM_BK / 2));
                     if (BN > UM_MAX_BN) {
                         // tokens 256.. of the tile: rows 256.. of the B stage (1 KB swizzle atoms)
@@ -419,7 +472,32 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             break;
                         }
                         uint32_t v[32];
-                        Dec::decode(raw_ring + r * Dec::RAW, arow, kc, v);
+                        if (K2) {
+                            // 128-k stage: each half decoded and stored in turn (one
+                            // 32-register array; its store completes before reuse)
+                            if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
+                                *abort_flag = 1;
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t acol = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)s * A_COLS;
+                            Dec::decode2(raw_ring + r * RAWB, arow, kc, 0, v);
+                            tmem_st_32x32b_x32(acol, v);
+                            tmem_wait_st();
+                            Dec::decode2(raw_ring + r * RAWB, arow, kc, 1, v);
+                            __syncwarp();                      // raw reads done: release the slot
+                            if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
+                            tmem_st_32x32b_x32(acol + (uint32_t)(UM_BK / 2), v);
+                            tmem_wait_st();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->full[s]);
+                            if (++s == S) { s = 0; ph ^= 1u; }
+                            if (++r == SR) { r = 0; rph ^= 1u; }
+                            continue;
+                        }
+                        Dec::decode(raw_ring + r * RAWB, arow, kc, v);
                         // no proxy fence before releasing the slot: its reads
                         // are ordered before the (release) arrive, and the TMA
                         // that refills it is issued after the producer's wait
@@ -546,11 +624,15 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 // to share its activation tile (192 rows each by multicast: a TMA box is at
 // most 256 rows); pairing at 256 tokens measured slower (a multicast tile
 // lands at about half the rate of one a CTA loads alone).
-template <class Dec, int MODE, bool AT>
+template <class Dec, int MODE, bool AT, bool K2>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
     const bool wide = BN == UM_WIDE_BN;
     if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide) || (wide && !AT))
+        return cudaErrorInvalidValue;
+    constexpr int KA = K2 ? 2 : 1;
+    // 128-k stages: tensor-memory A, no clusters, every K split at least one stage
+    if (K2 && (!AT || wide || Dec::DIRECT || K % (UM_BK * KA) != 0 || splits > K / (UM_BK * KA)))
         return cudaErrorInvalidValue;
     // the epilogue drains 32 columns at a time: a tile narrower than a
     // multiple of 32 must be the only token tile
@@ -571,12 +653,15 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     const int NACC = wide ? 1 : 2;
     const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024;
     const int a_stage = AT ? 0 : UM_A_STAGE;
-    const int raw = Dec::DIRECT ? 0 : Dec::RAW;
+    const int raw = Dec::DIRECT ? 0 : (K2 ? Dec::RAW2 : Dec::RAW);
+    const int b_stage = BN * 128 * KA;
+    const int a_cols = UM_BK / 2 * KA;                    // tensor-memory columns of an A stage (AT)
     int S = UM_STAGES;
-    if (AT && S > (512 - NACC * BN) / (UM_BK / 2)) S = (512 - NACC * BN) / (UM_BK / 2);   // A ring in tensor memory
+    if (AT && S > (512 - NACC * BN) / a_cols) S = (512 - NACC * BN) / a_cols;   // A ring in tensor memory
     // leave room for at least 8 raw stages
-    while (S > 2 && (size_t)S * (BN * 128 + a_stage) + (size_t)8 * raw > budget) --S;
-    int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (BN * 128 + a_stage)) / (size_t)(raw > 0 ? raw : 1));
+    while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)8 * raw > budget) --S;
+    if (K2 && S < 2) return cudaErrorInvalidValue;
+    int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
     if (SR > UM_RAW_STAGES) SR = UM_RAW_STAGES;
     // an even depth: the two decoder warps of a quarter take alternate items,
     // so items it and it + SR (one raw slot) belong to the same warp and no
@@ -584,12 +669,12 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     SR &= ~1;
     if (SR < 2) return cudaErrorInvalidValue;
     int tmem_cols = 32;
-    while (tmem_cols < NACC * BN + (AT ? S * (UM_BK / 2) : 0)) tmem_cols <<= 1;
+    while (tmem_cols < NACC * BN + (AT ? S * a_cols : 0)) tmem_cols <<= 1;
     if (tmem_cols > 512) return cudaErrorInvalidValue;
     // At least 120 KB of shared memory: no two CTAs of this kernel can share
     // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
     // (which a cluster barrier could otherwise turn into a deadlock).
-    size_t smem = (size_t)S * (BN * 128 + a_stage) + (Dec::DIRECT ? 0 : (size_t)SR * raw) + 1024 + sizeof(UmmaBars) +
+    size_t smem = (size_t)S * (b_stage + a_stage) + (Dec::DIRECT ? 0 : (size_t)SR * raw) + 1024 + sizeof(UmmaBars) +
                   1024;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
@@ -598,13 +683,13 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     tm.tiles_m = (T + BN - 1) / BN;
     tm.splits = splits;
     tm.total = tm.tiles_np * tm.tiles_m * splits;
-    tm.nk_total = K / UM_BK;
+    tm.nk_total = K / (UM_BK * KA);
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int units = tm.total < sms / cl ? tm.total : sms / cl;
-    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT, K2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * cl));
@@ -620,16 +705,21 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols, tm,
-                              S, SR, NACC, cl);
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, K2>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols,
+                              tm, S, SR, NACC, cl);
 }
 
 template <class Dec, int MODE>
 cudaError_t launch_umma(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                         int splits, cudaStream_t st) {
-    if ((BN <= 128 || BN == UM_WIDE_BN) && !Dec::DIRECT)
-        return launch_umma_impl<Dec, MODE, true>(pm, ep, act16, T, R, K, BN, splits, st);
-    return launch_umma_impl<Dec, MODE, false>(pm, ep, act16, T, R, K, BN, splits, st);
+    if constexpr (!Dec::DIRECT) {
+        // token tiles of at most 128: 128-k stages when every K split keeps one
+        if (BN <= 128 && K % (2 * UM_BK) == 0 && splits <= K / (2 * UM_BK))
+            return launch_umma_impl<Dec, MODE, true, true>(pm, ep, act16, T, R, K, BN, splits, st);
+        if (BN <= 128 || BN == UM_WIDE_BN)
+            return launch_umma_impl<Dec, MODE, true, false>(pm, ep, act16, T, R, K, BN, splits, st);
+    }
+    return launch_umma_impl<Dec, MODE, false, false>(pm, ep, act16, T, R, K, BN, splits, st);
 }
 
 inline int umma_pick_bn(int T) {
