@@ -84,19 +84,24 @@ struct DecTQ2 {
         tma_load_3d(raw, m0, bar, 0, kc * 16, row0 >> 7);     // codes: 16 lines of 128 B
         tma_load_2d(raw + UM_BM * 16, m1, bar, row0, kc / 2);   // scales: x = row, y = block
     }
-    // a 128-k stage (one block): codes [2][128 rows][16 B], then the block's scales
-    static constexpr int RAW2 = UM_BM * 32 + UM_BM * 2;
-    __device__ __forceinline__ static void issue2(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* raw,
-                                                  uint64_t* bar, int row0, int kb) {
-        tma_load_3d(raw, m0, bar, 0, kb * 32, row0 >> 7);
-        tma_load_3d(raw + UM_BM * 16, m0, bar, 0, kb * 32 + 16, row0 >> 7);
-        tma_load_2d(raw + UM_BM * 32, m1, bar, row0, kb);
+    // a stage of KA = 2 or 4 atoms of 64 k (one or two blocks): codes
+    // [KA][128 rows][16 B], then the blocks' scales [KA/2][128 rows]
+    template <int KA>
+    __host__ __device__ static constexpr int rawk() { return UM_BM * 16 * KA + UM_BM * 2 * (KA / 2); }
+    template <int KA>
+    __device__ __forceinline__ static void issuek(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* raw,
+                                                  uint64_t* bar, int row0, int ks) {
+#pragma unroll
+        for (int p = 0; p < KA; ++p) tma_load_3d(raw + p * (UM_BM * 16), m0, bar, 0, (ks * KA + p) * 16, row0 >> 7);
+#pragma unroll
+        for (int b = 0; b < KA / 2; ++b)
+            tma_load_2d(raw + KA * (UM_BM * 16) + b * (UM_BM * 2), m1, bar, row0, ks * (KA / 2) + b);
     }
-    // half hf (k 64*hf .. 64*hf+63) of row r of a 128-k stage
-    __device__ __forceinline__ static void decode2(const uint8_t* raw, int r, int kb, int hf, uint32_t (&v)[32]) {
-        expand(*reinterpret_cast<const uint4*>(raw + hf * (UM_BM * 16) + r * 16),
-               reinterpret_cast<const uint16_t*>(raw + UM_BM * 32)[r], v);
-        (void)kb;
+    // atom p (k 64p .. 64p+63 of the stage) of row r
+    template <int KA>
+    __device__ __forceinline__ static void decodek(const uint8_t* raw, int r, int p, uint32_t (&v)[32]) {
+        expand(*reinterpret_cast<const uint4*>(raw + p * (UM_BM * 16) + r * 16),
+               reinterpret_cast<const uint16_t*>(raw + KA * (UM_BM * 16) + (p >> 1) * (UM_BM * 2))[r], v);
     }
     __device__ __forceinline__ static void decode(const uint8_t* raw, int r, int kc, uint32_t (&v)[32]) {
         expand(*reinterpret_cast<const uint4*>(raw + r * 16), reinterpret_cast<const uint16_t*>(raw + UM_BM * 16)[r],
@@ -146,15 +151,18 @@ struct DecSign {
         word(w.x, v);
         word(w.y, v + 16);
     }
-    // a 128-k stage: the same four words a row
-    static constexpr int RAW2 = UM_BM * 16;
-    __device__ __forceinline__ static void issue2(const CUtensorMap* m0, const CUtensorMap*, uint8_t* raw,
-                                                  uint64_t* bar, int row0, int kb) {
-        tma_load_2d(raw, m0, bar, kb * 4, row0);
+    // a stage of KA = 2 or 4 atoms of 64 k: KA/2 boxes [128 rows][4 words]
+    template <int KA>
+    __host__ __device__ static constexpr int rawk() { return UM_BM * 8 * KA; }
+    template <int KA>
+    __device__ __forceinline__ static void issuek(const CUtensorMap* m0, const CUtensorMap*, uint8_t* raw,
+                                                  uint64_t* bar, int row0, int ks) {
+#pragma unroll
+        for (int b = 0; b < KA / 2; ++b) tma_load_2d(raw + b * (UM_BM * 16), m0, bar, (ks * (KA / 2) + b) * 4, row0);
     }
-    __device__ __forceinline__ static void decode2(const uint8_t* raw, int r, int kb, int hf, uint32_t (&v)[32]) {
-        decode(raw, r, hf, v);
-        (void)kb;
+    template <int KA>
+    __device__ __forceinline__ static void decodek(const uint8_t* raw, int r, int p, uint32_t (&v)[32]) {
+        decode(raw + (p >> 1) * (UM_BM * 16), r, p & 1, v);
     }
 };
 
@@ -168,10 +176,8 @@ struct DecDense {
         tma_load_2d(a_stage, m0, bar, kc * UM_BK, row0);
     }
     __device__ __forceinline__ static void decode(const uint8_t*, int, int, uint32_t (&)[32]) {}
-    static constexpr int RAW2 = 0;   // no 128-k stages (the shared-memory A path only)
-    __device__ __forceinline__ static void issue2(const CUtensorMap*, const CUtensorMap*, uint8_t*, uint64_t*, int,
-                                                  int) {}
-    __device__ __forceinline__ static void decode2(const uint8_t*, int, int, int, uint32_t (&)[32]) {}
+    template <int KA>
+    __host__ __device__ static constexpr int rawk() { return 0; }   // one-atom stages only (the shared-memory A path)
 };
 
 // Host side: the tensor maps a plane's decoder loads from (PlaneMaps,
@@ -247,19 +253,18 @@ struct TileMap {
 // columns a stage after the NACC accumulators) instead of shared memory, and
 // the MMAs read A from there; for token tiles of at most 128, where the
 // shared-memory round trip of the decoded rows would cost more than the MMAs.
-// K2 (with AT): a pipeline stage spans 128 k (two 64-k swizzle atoms of
-// activations, 64 tensor-memory columns of A, eight MMAs), which halves the
-// per-stage waits, commits and hand-offs that set the pace of narrow token
-// tiles; the MMA sequence, and so the result, is that of two 64-k stages.
-template <class Dec, int MODE, bool AT, bool K2 = false>
+// KA > 1 (with AT): a pipeline stage spans KA x 64 k (KA 64-k swizzle atoms
+// of activations, 32 KA tensor-memory columns of A, 4 KA MMAs), which cuts
+// the per-stage waits, commits and hand-offs that set the pace of narrow
+// token tiles; the MMA sequence, and so the result, is that of KA 64-k stages.
+template <class Dec, int MODE, bool AT, int KA = 1>
 __global__ void __launch_bounds__(UM_THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap0,
                  const __grid_constant__ CUtensorMap amap1, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
                  const TileMap tm, int S, int SR, int NACC, int cl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int KA = K2 ? 2 : 1;                       // 64-k atoms a stage
-    constexpr int RAWB = K2 ? Dec::RAW2 : Dec::RAW;      // raw plane bytes a stage
+    constexpr int RAWB = KA > 1 ? Dec::template rawk<KA>() : Dec::RAW;   // raw plane bytes a stage
     const int stage_bytes = BN * 128 * KA;               // [KA][BN rows][128 B]
     uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned (!AT)
     uint8_t* raw_ring = a_ring + (AT ? 0 : S * UM_A_STAGE);          // [SR][RAWB] (!DIRECT)
@@ -359,8 +364,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         break;
                     }
                     mbar_arrive_expect_tx(&bars->raw_full[r], (uint32_t)RAWB);
-                    if (K2) Dec::issue2(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
-                    else Dec::issue(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
+                    if constexpr (KA > 1)
+                        Dec::template issuek<KA>(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
+                    else
+                        Dec::issue(&amap0, &amap1, raw_ring + r * RAWB, &bars->raw_full[r], row0, kc);
                     if (++r == SR) { r = 0; ph ^= 1u; }
                 }
             }
@@ -406,7 +413,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 ready = mbar_test_wait(&bars->full[s1], ph1);   // its latency hides under the MMAs below
                 tc_fence_after();
                 const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * stage_bytes));
-                if (AT && K2) {
+                if (AT && KA > 1) {
                     // atom a of the B stage at a * BN rows; k-step j of atom a at A column (4a + j) * 8
                     const uint32_t acol = tmem + a_col0 + (uint32_t)s * A_COLS;
 #pragma unroll
@@ -472,9 +479,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             break;
                         }
                         uint32_t v[32];
-                        if (K2) {
-                            // 128-k stage: each half decoded and stored in turn (one
-                            // 32-register array; its store completes before reuse)
+                        if constexpr (KA > 1) {
+                            // multi-atom stage: each 64-k atom decoded and stored in
+                            // turn (one 32-register array; its store completes
+                            // before the array is reused)
                             if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                                 *abort_flag = 1;
                                 ok = false;
@@ -482,14 +490,16 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             }
                             tc_fence_after();
                             const uint32_t acol = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)s * A_COLS;
-                            Dec::decode2(raw_ring + r * RAWB, arow, kc, 0, v);
-                            tmem_st_32x32b_x32(acol, v);
-                            tmem_wait_st();
-                            Dec::decode2(raw_ring + r * RAWB, arow, kc, 1, v);
-                            __syncwarp();                      // raw reads done: release the slot
-                            if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
-                            tmem_st_32x32b_x32(acol + (uint32_t)(UM_BK / 2), v);
-                            tmem_wait_st();
+#pragma unroll
+                            for (int p = 0; p < KA; ++p) {
+                                Dec::template decodek<KA>(raw_ring + r * RAWB, arow, p, v);
+                                if (p == KA - 1) {
+                                    __syncwarp();              // raw reads done: release the slot
+                                    if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
+                                }
+                                tmem_st_32x32b_x32(acol + (uint32_t)(p * (UM_BK / 2)), v);
+                                tmem_wait_st();
+                            }
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&bars->full[s]);
@@ -624,15 +634,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 // to share its activation tile (192 rows each by multicast: a TMA box is at
 // most 256 rows); pairing at 256 tokens measured slower (a multicast tile
 // lands at about half the rate of one a CTA loads alone).
-template <class Dec, int MODE, bool AT, bool K2>
+template <class Dec, int MODE, bool AT, int KA>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
     const bool wide = BN == UM_WIDE_BN;
     if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide) || (wide && !AT))
         return cudaErrorInvalidValue;
-    constexpr int KA = K2 ? 2 : 1;
-    // 128-k stages: tensor-memory A, no clusters, every K split at least one stage
-    if (K2 && (!AT || wide || Dec::DIRECT || K % (UM_BK * KA) != 0 || splits > K / (UM_BK * KA)))
+    // multi-atom stages: tensor-memory A, no clusters, every K split at least one stage
+    if (KA > 1 && (!AT || wide || Dec::DIRECT || K % (UM_BK * KA) != 0 || splits > K / (UM_BK * KA)))
         return cudaErrorInvalidValue;
     // the epilogue drains 32 columns at a time: a tile narrower than a
     // multiple of 32 must be the only token tile
@@ -653,14 +662,14 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     const int NACC = wide ? 1 : 2;
     const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024;
     const int a_stage = AT ? 0 : UM_A_STAGE;
-    const int raw = Dec::DIRECT ? 0 : (K2 ? Dec::RAW2 : Dec::RAW);
+    const int raw = Dec::DIRECT ? 0 : (KA > 1 ? Dec::template rawk<KA>() : Dec::RAW);
     const int b_stage = BN * 128 * KA;
     const int a_cols = UM_BK / 2 * KA;                    // tensor-memory columns of an A stage (AT)
     int S = UM_STAGES;
     if (AT && S > (512 - NACC * BN) / a_cols) S = (512 - NACC * BN) / a_cols;   // A ring in tensor memory
     // leave room for at least 8 raw stages
     while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)8 * raw > budget) --S;
-    if (K2 && S < 2) return cudaErrorInvalidValue;
+    if (KA > 1 && S < 2) return cudaErrorInvalidValue;
     int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
     if (SR > UM_RAW_STAGES) SR = UM_RAW_STAGES;
     // an even depth: the two decoder warps of a quarter take alternate items,
@@ -688,7 +697,7 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int units = tm.total < sms / cl ? tm.total : sms / cl;
-    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT, K2>,
+    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT, KA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -705,7 +714,7 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, K2>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols,
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, KA>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols,
                               tm, S, SR, NACC, cl);
 }
 
@@ -713,13 +722,18 @@ template <class Dec, int MODE>
 cudaError_t launch_umma(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                         int splits, cudaStream_t st) {
     if constexpr (!Dec::DIRECT) {
-        // token tiles of at most 128: 128-k stages when every K split keeps one
+        // token tiles of at most 128: stages of 256 k (tensor memory holds
+        // two to three of them after the accumulators: at 32 tokens 19.6 ->
+        // 16.6 us and at 128 tokens 20.5 -> 19.6 us against 128-k stages, at
+        // N=11008, K=4096), else 128 k, when every K split keeps at least one
+        if (BN <= 128 && K % (4 * UM_BK) == 0 && splits <= K / (4 * UM_BK))
+            return launch_umma_impl<Dec, MODE, true, 4>(pm, ep, act16, T, R, K, BN, splits, st);
         if (BN <= 128 && K % (2 * UM_BK) == 0 && splits <= K / (2 * UM_BK))
-            return launch_umma_impl<Dec, MODE, true, true>(pm, ep, act16, T, R, K, BN, splits, st);
+            return launch_umma_impl<Dec, MODE, true, 2>(pm, ep, act16, T, R, K, BN, splits, st);
         if (BN <= 128 || BN == UM_WIDE_BN)
-            return launch_umma_impl<Dec, MODE, true, false>(pm, ep, act16, T, R, K, BN, splits, st);
+            return launch_umma_impl<Dec, MODE, true, 1>(pm, ep, act16, T, R, K, BN, splits, st);
     }
-    return launch_umma_impl<Dec, MODE, false, false>(pm, ep, act16, T, R, K, BN, splits, st);
+    return launch_umma_impl<Dec, MODE, false, 1>(pm, ep, act16, T, R, K, BN, splits, st);
 }
 
 inline int umma_pick_bn(int T) {
