@@ -322,7 +322,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 int np, m, z;
                 tm.decode(t, np, m, z);
                 const int row0 = (np * cl + rank) * UM_BM;
-                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
+                const int k1 = tm.kc1(z);
+                for (int kc = tm.kc0(z); kc < k1; ++kc, ++it) {
                     if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
                         ok = false;
@@ -357,7 +358,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 int np, m, z;
                 tm.decode(t, np, m, z);
                 const int row0 = (np * cl + rank) * UM_BM;
-                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
+                const int k1 = tm.kc1(z);
+                for (int kc = tm.kc0(z); kc < k1; ++kc, ++it) {
                     if (it >= SR && !mbar_wait_or_abort(&bars->raw_empty[r], ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
                         ok = false;
@@ -461,52 +463,58 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         }
     } else if (warp >= 4 && warp < 12) {                   // ---- decoders
         if (!Dec::DIRECT) {
-            // warp pair (q, h): lane quarter q, stages with item parity h; a
-            // stage's raw tile is in shared memory (it landed S_R stages ahead)
+            // warp pair (q, h): lane quarter q, the items (stages) of parity h
+            // of the CTA's item sequence; the loop visits only those.  A
+            // stage's raw tile is in shared memory (it landed S_R stages ahead).
             const int q = warp & 3, h = (warp - 4) >> 2;
             const int arow = q * 32 + lane;                // row of the tile this thread decodes
             int it = 0, s = 0, r = 0;
             uint32_t ph = 0, rph = 0;                      // A-ring and raw-ring phase parities of item `it`
+            auto advance = [&](int n) {                    // n <= 2 <= S, SR
+                it += n;
+                s += n;
+                if (s >= S) { s -= S; ph ^= 1u; }
+                r += n;
+                if (r >= SR) { r -= SR; rph ^= 1u; }
+            };
+            if (h) advance(1);
+            int lead = h;                                  // first own item's offset into the next tile
             bool ok = true;
             for (int t = unit0; t < tm.total && ok; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
-                for (int kc = tm.kc0(z); kc < tm.kc1(z); ++kc, ++it) {
-                    if ((it & 1) == h) {
-                        if (!mbar_wait_or_abort(&bars->raw_full[r], rph, abort_flag)) {
+                const int k1 = tm.kc1(z);
+                int kc = tm.kc0(z) + lead;
+                for (; kc < k1; kc += 2, advance(2)) {
+                    if (!mbar_wait_or_abort(&bars->raw_full[r], rph, abort_flag)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    uint32_t v[32];
+                    if constexpr (KA > 1) {
+                        // multi-atom stage: each 64-k atom decoded and stored in
+                        // turn (one 32-register array; its store completes
+                        // before the array is reused)
+                        if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                             *abort_flag = 1;
                             ok = false;
                             break;
                         }
-                        uint32_t v[32];
-                        if constexpr (KA > 1) {
-                            // multi-atom stage: each 64-k atom decoded and stored in
-                            // turn (one 32-register array; its store completes
-                            // before the array is reused)
-                            if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
-                                *abort_flag = 1;
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t acol = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)s * A_COLS;
+                        tc_fence_after();
+                        const uint32_t acol = tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (uint32_t)s * A_COLS;
 #pragma unroll
-                            for (int p = 0; p < KA; ++p) {
-                                Dec::template decodek<KA>(raw_ring + r * RAWB, arow, p, v);
-                                if (p == KA - 1) {
-                                    __syncwarp();              // raw reads done: release the slot
-                                    if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
-                                }
-                                tmem_st_32x32b_x32(acol + (uint32_t)(p * (UM_BK / 2)), v);
-                                tmem_wait_st();
+                        for (int p = 0; p < KA; ++p) {
+                            Dec::template decodek<KA>(raw_ring + r * RAWB, arow, p, v);
+                            if (p == KA - 1) {
+                                __syncwarp();                  // raw reads done: release the slot
+                                if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
                             }
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&bars->full[s]);
-                            if (++s == S) { s = 0; ph ^= 1u; }
-                            if (++r == SR) { r = 0; rph ^= 1u; }
-                            continue;
+                            tmem_st_32x32b_x32(acol + (uint32_t)(p * (UM_BK / 2)), v);
+                            tmem_wait_st();
                         }
+                        tc_fence_before();
+                    } else {
                         Dec::decode(raw_ring + r * RAWB, arow, kc, v);
                         // no proxy fence before releasing the slot: its reads
                         // are ordered before the (release) arrive, and the TMA
@@ -535,12 +543,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                                     make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
                             fence_proxy_async_shared();    // the MMA reads A through the async proxy
                         }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->full[s]);
                     }
-                    if (++s == S) { s = 0; ph ^= 1u; }
-                    if (++r == SR) { r = 0; rph ^= 1u; }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->full[s]);
                 }
+                lead = kc - k1;                            // 0, or 1 when the tile's last item was not ours
             }
         }
     } else if (warp >= 12) {                               // ---- epilogue
