@@ -361,6 +361,34 @@ def test_tensor_tuned_tiles_and_splits(lib):
             lib.tq2_gemm_tensor_tuned(w, x, out, bn, splits)
 
 
+def test_tensor_stage_widths(lib):
+    """Token tiles of at most 128 run pipeline stages of four, two or one
+    64-k atoms: four while every K split keeps a 256-k stage, else two while
+    it keeps a 128-k stage, else one.  K = 768 takes four atoms up to three
+    splits, two at four to six and one at seven to twelve; ragged row and
+    token tiles throughout, each within the tensor bound against the oracle,
+    two splits bit-equal to one another run to run."""
+    import torch
+    N, K = 300, 768
+    aos = synth.random_tq2(N, K, 150)
+    w = lib.tq2_upload(aos, N, K)
+    for M, tiles in ((33, (48, 64)), (100, (32, 128))):
+        x = synth.random_x(M, K, 151 + M)
+        ref, absref, ref16, absref16 = oracle_gemm(aos, N, K, x)
+        xd = to_dev(x)
+        for bn in tiles:
+            for splits in (1, 2, 3, 4, 6, 7, 12):
+                out = torch.full((M, N), float("nan"), device="cuda")
+                lib.tq2_gemm_tensor_tuned(w, xd, out, bn, splits)
+                lib.device_status()
+                got = out.cpu().numpy().astype(np.float64)
+                check_tensor(got, ref, absref, ref16, absref16, f"stages M={M} bn={bn} splits={splits}")
+                if splits <= 2:
+                    again = torch.full((M, N), float("nan"), device="cuda")
+                    lib.tq2_gemm_tensor_tuned(w, xd, again, bn, splits)
+                    assert torch.equal(out, again), (M, bn, splits)
+
+
 def test_tensor_large_sampled(lib):
     """M=4096, N=14336, K=4096 in the benchmarked launch configuration; the
     oracle computes sampled outputs one by one (random elements plus two full
