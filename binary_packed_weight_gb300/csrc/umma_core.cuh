@@ -47,6 +47,13 @@ constexpr int UM_A_STAGE = UM_BM * UM_BK * 2;   // decoded weight stage in share
 // warps 4-11 decoders (two per 32-row quarter of the tile, taking alternate stages),
 // warps 12-15 epilogue (one per lane quarter)
 constexpr int UM_THREADS = 512;
+// TMA epilogue: an input ring of UM_EPI_IN chunks of [32 tokens][128 rows]
+// f32 (the column-sum operand), and per epilogue warp two output buffers of
+// [32 tokens][32 rows] f32 stored by TMA
+constexpr int UM_EPI_IN = 4;
+constexpr int UM_EPI_IN_BYTES = 32 * UM_BM * 4;             // 16 KB
+constexpr int UM_EPI_OUT_BYTES = 4 * 2 * 32 * 32 * 4;       // 32 KB
+constexpr int UM_EPI_TMA_STEPS = 16;                        // K / 64 at most for the TMA epilogue
 
 struct UmmaBars {
     uint64_t full[UM_STAGES];      // a stage's B tile landed (TMA bytes) and its A rows are decoded (4 warps)
@@ -55,6 +62,8 @@ struct UmmaBars {
     uint64_t raw_empty[UM_RAW_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    uint64_t epi_full[UM_EPI_IN];  // TMA epilogue: a 32-token chunk of the epilogue's input landed
+    uint64_t epi_empty[UM_EPI_IN]; // ... and the four epilogue warps are done with it
     uint32_t tmem_base;
     int abort;
 };
@@ -260,8 +269,9 @@ struct TileMap {
 template <class Dec, int MODE, bool AT, int KA = 1>
 __global__ void __launch_bounds__(UM_THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap0,
-                 const __grid_constant__ CUtensorMap amap1, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
-                 const TileMap tm, int S, int SR, int NACC, int cl) {
+                 const __grid_constant__ CUtensorMap amap1, const __grid_constant__ CUtensorMap omap,
+                 const __grid_constant__ CUtensorMap imap, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
+                 const TileMap tm, int S, int SR, int NACC, int cl, int et) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int RAWB = KA > 1 ? Dec::template rawk<KA>() : Dec::RAW;   // raw plane bytes a stage
@@ -269,6 +279,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     uint8_t* a_ring = smem + S * stage_bytes;            // [S][128 rows][128 B], swizzled; 1 KB aligned (!AT)
     uint8_t* raw_ring = a_ring + (AT ? 0 : S * UM_A_STAGE);          // [SR][RAWB] (!DIRECT)
     UmmaBars* bars = reinterpret_cast<UmmaBars*>(raw_ring + (Dec::DIRECT ? 0 : SR * RAWB));
+    // TMA epilogue (et): its input ring (column-sum modes) then the output
+    // buffers (storing modes), 1 KB aligned after the barriers
+    constexpr bool EPI_IN = MODE == EPI_COLSUM || MODE == EPI_SCALE_COLSUM;
+    constexpr bool EPI_OUT = MODE != EPI_COLSUM;
+    float* epi_in = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(bars) + sizeof(UmmaBars) + 1023) & ~uintptr_t(1023));
+    float* epi_out = epi_in + (EPI_IN ? UM_EPI_IN * UM_EPI_IN_BYTES / 4 : 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
     // tiles of the same unit and share its activation tile: each loads 1/cl
@@ -290,11 +307,17 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             mbar_init(&bars->acc_full[b], 1);
             mbar_init(&bars->acc_empty[b], 4);
         }
+        for (int e = 0; e < UM_EPI_IN; ++e) {
+            mbar_init(&bars->epi_full[e], 1);
+            mbar_init(&bars->epi_empty[e], 4);
+        }
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&amap0);
         if (!Dec::DIRECT) tma_prefetch_desc(&amap1);
+        if (et && EPI_OUT) tma_prefetch_desc(&omap);
+        if (et && EPI_IN) tma_prefetch_desc(&imap);
     }
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, (uint32_t)tmem_cols);
@@ -347,6 +370,32 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             // let the copies already issued land before the CTA can exit
             for (int i = (it > S ? it - S : 0); i < it; ++i)
                 mbar_wait(&bars->full[i % S], (uint32_t)(i / S) & 1u);
+        }
+    } else if (warp == 2) {
+        if (EPI_IN && et && lane == 0) {                   // ---- TMA epilogue input producer
+            // the column-sum operand, 32 tokens x 128 rows a chunk, in the
+            // order the epilogue warps consume it
+            pdl_wait();
+            int c = 0, e = 0;
+            uint32_t eph = 0;
+            bool ok = true;
+            for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
+                int np, m, z;
+                tm.decode(t, np, m, z);
+                for (int cc = 0; cc < BN; cc += 32, ++c) {
+                    if (c >= UM_EPI_IN && !mbar_wait_or_abort(&bars->epi_empty[e], eph ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->epi_full[e], (uint32_t)UM_EPI_IN_BYTES);
+                    tma_load_2d(epi_in + e * (UM_EPI_IN_BYTES / 4), &imap, &bars->epi_full[e], np * UM_BM,
+                                m * BN + cc);
+                    if (++e == UM_EPI_IN) { e = 0; eph ^= 1u; }
+                }
+            }
+            for (int i = (c > UM_EPI_IN ? c - UM_EPI_IN : 0); i < c; ++i)
+                mbar_wait(&bars->epi_full[i % UM_EPI_IN], (uint32_t)(i / UM_EPI_IN) & 1u);
         }
     } else if (warp == 3) {
         if (!Dec::DIRECT && lane == 0) {                   // ---- plane TMA producer (raw stages)
@@ -555,6 +604,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         bool waited = false;
         int lt = 0;
+        int ec = 0, e = 0, ob = 0;                         // TMA epilogue: chunk count, input slot, output buffer
+        uint32_t eph = 0;
         for (int t = unit0; t < tm.total; t += units, ++lt) {
             int np, m, z;
             tm.decode(t, np, m, z);
@@ -574,6 +625,69 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             const int m0 = m * BN;
             const float vs = (rok && (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM)) ? ep.vec[row] : 1.f;
             float colacc = 0.f;
+            if (et) {
+                // 32 tokens at a time: the column-sum operand from the input
+                // ring (this warp's 32 rows of the chunk), the results through
+                // a [32 tokens][32 rows] buffer and one TMA store (tokens past
+                // T and rows past R are neither read nor written)
+                bool fail = false;
+                for (int cc = 0; cc < BN; cc += 32, ++ec) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_addr + (uint32_t)(buf * BN + cc), v);
+                    tmem_wait_ld();
+                    if (cc + 32 >= BN) {                   // accumulator fully read: hand it back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->acc_empty[buf]);
+                    }
+                    const float* in = epi_in + e * (UM_EPI_IN_BYTES / 4) + q * 32 + lane;   // token i at in[128 i]
+                    float* o = epi_out + (q * 2 + ob) * 1024;                              // token i at o[32 i + lane]
+                    if (EPI_IN && !mbar_wait_or_abort(&bars->epi_full[e], eph, abort_flag)) {
+                        *abort_flag = 1;
+                        fail = true;
+                        break;
+                    }
+                    if (EPI_OUT) {
+                        if (lane == 0) bulk_wait_group_read<1>();   // this buffer's store (two chunks back) has read it
+                        __syncwarp();
+                    }
+                    // columns past the accumulator (a tile narrower than a
+                    // multiple of 32) hold other data: stored only where the
+                    // TMA clips them (tokens past T), and kept out of the sums
+                    const int nvalid = (T - (m0 + cc)) < 32 ? (T - (m0 + cc)) : 32;
+                    auto one = [&](int i, bool valid) {
+                        const float w = __uint_as_float(v[i]) * ep.oscale;
+                        if (MODE == EPI_STORE) o[32 * i + lane] = w;
+                        if (MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) o[32 * i + lane] = __fmul_rn(w, vs);
+                        if (EPI_IN && valid) colacc = fmaf(w, in[128 * i], colacc);
+                    };
+                    if (nvalid == 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) one(i, true);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) one(i, i < nvalid);
+                    }
+                    if (EPI_IN) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->epi_empty[e]);
+                        if (++e == UM_EPI_IN) { e = 0; eph ^= 1u; }
+                    }
+                    if (EPI_OUT) {
+                        fence_proxy_async_shared();        // the TMA store reads the buffer through the async proxy
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&omap, o, n * UM_BM + q * 32, m0 + cc);
+                            bulk_commit_group();
+                        }
+                        ob ^= 1;
+                    }
+                }
+                if (fail) break;
+                if ((MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) && rok)
+                    ep.colpart[(int64_t)m * ep.ldo + row] = colacc;
+                continue;
+            }
             for (int cc = 0; cc < BN; cc += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_addr + (uint32_t)(buf * BN + cc), v);
@@ -619,6 +733,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             if ((MODE == EPI_SCALE_COLSUM || MODE == EPI_COLSUM) && rok)
                 ep.colpart[(int64_t)m * ep.ldo + row] = colacc;
         }
+        if (et && EPI_OUT && lane == 0) bulk_wait_group<0>();   // this warp's stores are complete
     }
 
     tc_fence_before();
@@ -667,23 +782,51 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     // the A ring takes S x 32 tensor-memory columns after the accumulators
     // (2 x 128 + 8 x 32 or 384 + 4 x 32 = 512 at most)
     const int NACC = wide ? 1 : 2;
-    const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024;
     const int a_stage = AT ? 0 : UM_A_STAGE;
     const int raw = Dec::DIRECT ? 0 : (KA > 1 ? Dec::template rawk<KA>() : Dec::RAW);
     const int b_stage = BN * 128 * KA;
     const int a_cols = UM_BK / 2 * KA;                    // tensor-memory columns of an A stage (AT)
-    int S = UM_STAGES;
-    if (AT && S > (512 - NACC * BN) / a_cols) S = (512 - NACC * BN) / a_cols;   // A ring in tensor memory
-    // leave room for at least 8 raw stages
-    while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)8 * raw > budget) --S;
-    if (KA > 1 && S < 2) return cudaErrorInvalidValue;
-    int SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
-    if (SR > UM_RAW_STAGES) SR = UM_RAW_STAGES;
-    // an even depth: the two decoder warps of a quarter take alternate items,
-    // so items it and it + SR (one raw slot) belong to the same warp and no
-    // warp can wait on a slot's phase a ring round ahead of its filling
-    SR &= ~1;
-    if (SR < 2) return cudaErrorInvalidValue;
+    // TMA epilogue (et) for GEMMs of at most UM_EPI_TMA_STEPS 64-k steps a
+    // tile, whose epilogue is not hidden behind the next tile's MMAs: plain
+    // stores and scaled stores without a second output or accumulation, and
+    // the column sums; needs 16-byte rows and bases, no clusters, no K split
+    constexpr bool EPI_IN = MODE == EPI_COLSUM || MODE == EPI_SCALE_COLSUM;
+    constexpr bool EPI_OUT = MODE != EPI_COLSUM;
+    const bool epi_mode = MODE == EPI_STORE || MODE == EPI_COLSUM ||
+                          ((MODE == EPI_SCALE || MODE == EPI_SCALE_COLSUM) && !ep.out2 && !ep.accumulate);
+    const bool epi_aligned = ep.ldo % 4 == 0 && (!EPI_OUT || (reinterpret_cast<uintptr_t>(ep.out) & 15) == 0) &&
+                             (!EPI_IN || (reinterpret_cast<uintptr_t>(ep.other) & 15) == 0);
+    int et = (epi_mode && epi_aligned && cl == 1 && splits == 1 && K / UM_BK <= UM_EPI_TMA_STEPS) ? 1 : 0;
+    int S = 0, SR = 0;
+    size_t epi_bytes = 0;
+    for (;; et = 0) {
+        epi_bytes = et ? (size_t)(EPI_IN ? UM_EPI_IN * UM_EPI_IN_BYTES : 0) + (EPI_OUT ? UM_EPI_OUT_BYTES : 0) + 1024
+                       : 0;
+        const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024 - epi_bytes;
+        S = UM_STAGES;
+        if (AT && S > (512 - NACC * BN) / a_cols) S = (512 - NACC * BN) / a_cols;   // A ring in tensor memory
+        // leave room for at least 8 raw stages
+        while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)8 * raw > budget) --S;
+        SR = 0;
+        if ((size_t)S * (b_stage + a_stage) < budget)
+            SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
+        if (SR > UM_RAW_STAGES) SR = UM_RAW_STAGES;
+        // an even depth: the two decoder warps of a quarter take alternate items,
+        // so items it and it + SR (one raw slot) belong to the same warp and no
+        // warp can wait on a slot's phase a ring round ahead of its filling
+        SR &= ~1;
+        if ((S >= 2 && SR >= 2) || !et) break;
+    }
+    if (S < 2 || SR < 2) return cudaErrorInvalidValue;
+    CUtensorMap omap{}, imap{};
+    if (et && EPI_OUT &&
+        !make_tensor_map_2d(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ep.out, (uint64_t)ep.ldo, (uint64_t)T,
+                            (uint64_t)ep.ldo * 4, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (et && EPI_IN &&
+        !make_tensor_map_2d(&imap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(ep.other), (uint64_t)ep.ldo,
+                            (uint64_t)T, (uint64_t)ep.ldo * 4, (uint32_t)UM_BM, 32u, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     int tmem_cols = 32;
     while (tmem_cols < NACC * BN + (AT ? S * a_cols : 0)) tmem_cols <<= 1;
     if (tmem_cols > 512) return cudaErrorInvalidValue;
@@ -691,7 +834,7 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
     // (which a cluster barrier could otherwise turn into a deadlock).
     size_t smem = (size_t)S * (b_stage + a_stage) + (Dec::DIRECT ? 0 : (size_t)SR * raw) + 1024 + sizeof(UmmaBars) +
-                  1024;
+                  1024 + epi_bytes;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
     tm.tiles_n = tiles_n;
@@ -721,8 +864,8 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, KA>, xmap, pm.m0, pm.m1, ep, T, R, BN, tmem_cols,
-                              tm, S, SR, NACC, cl);
+    return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, KA>, xmap, pm.m0, pm.m1, omap, imap, ep, T, R, BN,
+                              tmem_cols, tm, S, SR, NACC, cl, et);
 }
 
 template <class Dec, int MODE>
