@@ -805,8 +805,10 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
         const size_t budget = (size_t)220 * 1024 - sizeof(UmmaBars) - 1024 - epi_bytes;
         S = UM_STAGES;
         if (AT && S > (512 - NACC * BN) / a_cols) S = (512 - NACC * BN) / a_cols;   // A ring in tensor memory
-        // leave room for at least 8 raw stages
-        while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)8 * raw > budget) --S;
+        // leave room for at least 8 raw stages (4 beside the TMA epilogue's
+        // buffers, where a third stage measured faster than four more raw
+        // slots: the blr backward 72 -> 70 us)
+        while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)(et ? 4 : 8) * raw > budget) --S;
         SR = 0;
         if ((size_t)S * (b_stage + a_stage) < budget)
             SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
