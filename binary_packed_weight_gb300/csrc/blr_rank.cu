@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
                 w[2 * c + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
             fence_proxy_async_shared();
-            __syncwarp();                                   // reads done: release the slot (no proxy fence
-            if (lane == 0) mbar_arrive(&bars->xempty[s]);   // for a read before the async refill)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xempty[s]);
             if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;
@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(BR_THREADS, 1) blr_rank_kernel(const __grid_co
                 const int it = tid + 128 * u, j = it % BR_BK, na = it / BR_BK;
                 wv[u] = *reinterpret_cast<const uint2*>(wst + j * (RB / 32) + 2 * na);
             }
-            __syncwarp();                                   // reads done: release the slot (no proxy fence
-            if (lane == 0) mbar_arrive(&bars->xempty[s]);   // for a read before the async refill)
+            fence_proxy_async_shared();                     // the slot is refilled through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xempty[s]);
             if (i >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 break;

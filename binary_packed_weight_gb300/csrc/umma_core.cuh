@@ -556,7 +556,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         for (int p = 0; p < KA; ++p) {
                             Dec::template decodek<KA>(raw_ring + r * RAWB, arow, p, v);
                             if (p == KA - 1) {
-                                __syncwarp();                  // raw reads done: release the slot
+                                fence_proxy_async_shared();    // raw reads done: the slot is refilled
+                                __syncwarp();                  // through the async proxy
                                 if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
                             }
                             tmem_st_32x32b_x32(acol + (uint32_t)(p * (UM_BK / 2)), v);
@@ -565,9 +566,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         tc_fence_before();
                     } else {
                         Dec::decode(raw_ring + r * RAWB, arow, kc, v);
-                        // no proxy fence before releasing the slot: its reads
-                        // are ordered before the (release) arrive, and the TMA
-                        // that refills it is issued after the producer's wait
+                        // the raw slot is refilled through the async proxy
+                        fence_proxy_async_shared();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->raw_empty[r]);
                         if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
