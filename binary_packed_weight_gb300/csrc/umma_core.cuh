@@ -669,6 +669,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         for (int i = 0; i < 32; ++i) one(i, i < nvalid);
                     }
                     if (EPI_IN) {
+                        fence_proxy_async_shared();        // the slot is refilled through the async proxy
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->epi_empty[e]);
                         if (++e == UM_EPI_IN) { e = 0; eph ^= 1u; }
