@@ -66,17 +66,18 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // The wide 384-token tile (a decoded stage feeds 1.5x the tokens, A in
-    // tensor memory) when the CTA pairs' rounds of tiles make it cheaper than
-    // 256 tokens a tile: per token it runs ~7 % faster (measured at M=1536,
-    // N=27648, K=3072), but its coarser tiles can leave a last round
-    // half-empty (at M=4096, N=14336 it needs 9 rounds for 8.1 rounds of
-    // work against 12 for 11.8).
+    // tensor memory, CTA pairs) only when its rounds of tiles cover fewer
+    // tokens than those of 256-token tiles: per token the two now run alike
+    // (163.9 against 163.8 us at M=1536, N=27648, K=3072, since 256-token
+    // tiles also keep A in tensor memory), and the wide tile's coarser tiles
+    // can leave a last round half-empty (at M=4096, N=14336: 313 against
+    // 285 us).
     int BN = umma_pick_bn(M);
     if (M >= UM_WIDE_BN && tiles_n >= 2) {
         const int pairs = sms / 2, np = (tiles_n + 1) / 2;
         const long long rounds_w = (np * ((M + UM_WIDE_BN - 1) / UM_WIDE_BN) + pairs - 1) / pairs;
         const long long rounds_n = (np * ((M + UM_MAX_BN - 1) / UM_MAX_BN) + pairs - 1) / pairs;
-        if (rounds_w * UM_WIDE_BN * 93 < rounds_n * UM_MAX_BN * 100) BN = UM_WIDE_BN;
+        if (rounds_w * UM_WIDE_BN < rounds_n * UM_MAX_BN) BN = UM_WIDE_BN;
     }
     if (bn_force > 0) BN = bn_force;
     const int tiles_m = (M + BN - 1) / BN;

@@ -761,7 +761,7 @@ template <class Dec, int MODE, bool AT, int KA>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
     const bool wide = BN == UM_WIDE_BN;
-    if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide) || (wide && !AT))
+    if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide && BN != UM_MAX_BN) || (wide && !AT))
         return cudaErrorInvalidValue;
     // multi-atom stages: tensor-memory A, no clusters, every K split at least one stage
     if (KA > 1 && (!AT || wide || Dec::DIRECT || K % (UM_BK * KA) != 0 || splits > K / (UM_BK * KA)))
@@ -782,7 +782,7 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     // in shared memory, then the raw plane ring with what is left; with AT
     // the A ring takes S x 32 tensor-memory columns after the accumulators
     // (2 x 128 + 8 x 32 or 384 + 4 x 32 = 512 at most)
-    const int NACC = wide ? 1 : 2;
+    const int NACC = (wide || (AT && BN > 128)) ? 1 : 2;   // one accumulator when A takes its room
     const int a_stage = AT ? 0 : UM_A_STAGE;
     const int raw = Dec::DIRECT ? 0 : (KA > 1 ? Dec::template rawk<KA>() : Dec::RAW);
     const int b_stage = BN * 128 * KA;
@@ -809,7 +809,8 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
         // leave room for at least 8 raw stages (4 beside the TMA epilogue's
         // buffers, where a third stage measured faster than four more raw
         // slots: the blr backward 72 -> 70 us)
-        while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)(et ? 4 : 8) * raw > budget) --S;
+        while (S > 2 && (size_t)S * (b_stage + a_stage) + (size_t)(et || (AT && BN > 128) ? 4 : 8) * raw > budget)
+            --S;
         SR = 0;
         if ((size_t)S * (b_stage + a_stage) < budget)
             SR = Dec::DIRECT ? 2 : (int)((budget - (size_t)S * (b_stage + a_stage)) / (size_t)(raw > 0 ? raw : 1));
@@ -885,6 +886,15 @@ cudaError_t launch_umma(const PlaneMaps& pm, const EpiArgs& ep, const void* act1
             return launch_umma_impl<Dec, MODE, true, 2>(pm, ep, act16, T, R, K, BN, splits, st);
         if (BN <= 128 || BN == UM_WIDE_BN)
             return launch_umma_impl<Dec, MODE, true, 1>(pm, ep, act16, T, R, K, BN, splits, st);
+        // 256 tokens, plain or split-K stores (the ternary GEMM): A in tensor
+        // memory too, in 128-k stages, with one 256-column accumulator (the
+        // tile's epilogue then holds the MMAs, a few % of a tile) and three
+        // 64 KB activation stages: M=4096 x N=14336 302 -> 287 us, DiT
+        // N=3072 29.5 -> 28.3 us.  The column-sum modes keep the
+        // shared-memory A path and its room for the TMA epilogue.
+        if ((MODE == EPI_STORE || MODE == EPI_ATOMIC) && BN == UM_MAX_BN && K % (2 * UM_BK) == 0 &&
+            splits <= K / (2 * UM_BK))
+            return launch_umma_impl<Dec, MODE, true, 2>(pm, ep, act16, T, R, K, BN, splits, st);
     }
     return launch_umma_impl<Dec, MODE, false, 1>(pm, ep, act16, T, R, K, BN, splits, st);
 }
