@@ -339,7 +339,7 @@ def test_tensor_tuned_tiles_and_splits(lib):
     N, K = 300, 640
     aos = synth.random_tq2(N, K, 130)
     w = lib.tq2_upload(aos, N, K)
-    for M, tiles in ((33, (48, 64, 128)), (100, (32, 64, 128, 256, 384)), (600, (384,))):
+    for M, tiles in ((33, (48, 64, 128)), (100, (32, 64, 128, 256, 384)), (600, (256, 384))):
         x = synth.random_x(M, K, 131 + M)
         ref, absref, ref16, absref16 = oracle_gemm(aos, N, K, x)
         xd = to_dev(x)
