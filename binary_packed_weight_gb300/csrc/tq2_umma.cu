@@ -66,28 +66,25 @@ cudaError_t launch_tensor(const tq2_weight* w, const float* x, float* out, int M
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // The wide 384-token tile (a decoded stage feeds 1.5x the tokens, A in
-    // tensor memory, CTA pairs) only when its rounds of tiles cover fewer
-    // tokens than those of 256-token tiles: per token the two now run alike
-    // (163.9 against 163.8 us at M=1536, N=27648, K=3072, since 256-token
-    // tiles also keep A in tensor memory), and the wide tile's coarser tiles
-    // can leave a last round half-empty (at M=4096, N=14336: 313 against
-    // 285 us).
+    // tensor memory) only when its rounds of tiles cover fewer tokens than
+    // those of 256-token tiles: per token the two run alike (163.9 against
+    // 163.8 us at M=1536, N=27648, K=3072, both with A in tensor memory), and
+    // the wide tile's coarser tiles can leave a last round half-empty (at
+    // M=4096, N=14336: 313 against 285 us).
     int BN = umma_pick_bn(M);
-    if (M >= UM_WIDE_BN && tiles_n >= 2) {
-        const int pairs = sms / 2, np = (tiles_n + 1) / 2;
-        const long long rounds_w = (np * ((M + UM_WIDE_BN - 1) / UM_WIDE_BN) + pairs - 1) / pairs;
-        const long long rounds_n = (np * ((M + UM_MAX_BN - 1) / UM_MAX_BN) + pairs - 1) / pairs;
+    if (M >= UM_WIDE_BN) {
+        const long long rounds_w = ((long long)tiles_n * ((M + UM_WIDE_BN - 1) / UM_WIDE_BN) + sms - 1) / sms;
+        const long long rounds_n = ((long long)tiles_n * ((M + UM_MAX_BN - 1) / UM_MAX_BN) + sms - 1) / sms;
         if (rounds_w * UM_WIDE_BN < rounds_n * UM_MAX_BN) BN = UM_WIDE_BN;
     }
     if (bn_force > 0) BN = bn_force;
     const int tiles_m = (M + BN - 1) / BN;
     // K splits: 1 or 2 (two partials add into a zeroed output in either
     // order to the same sum); two only when they shorten the longest walk of
-    // a CTA (or CTA pair) over its units of work by a quarter or more: the
+    // a CTA over its units of work by a quarter or more: the
     // atomic epilogue reads and writes the output twice (at M=4096 x
     // N=14336 a 6 % shorter walk cost 28 % more time)
-    const int cl = (BN > UM_MAX_BN && tiles_n >= 2) ? 2 : 1;
-    const int slots = sms / cl, units1 = ((tiles_n + cl - 1) / cl) * tiles_m;
+    const int slots = sms, units1 = tiles_n * tiles_m;
     auto longest = [&](int sp) { return ((units1 * sp + slots - 1) / slots) * ((nk + sp - 1) / sp); };
     const int splits = splits_force > 0 ? splits_force : ((nk >= 4 && 4 * longest(2) <= 3 * longest(1)) ? 2 : 1);
 

@@ -243,8 +243,7 @@ struct EpiArgs {
 // continuously across tiles; the epilogue of a tile overlaps the MMAs of the
 // next.
 struct TileMap {
-    // a unit is `cl` weight tiles (one per CTA of a cluster) x one token tile
-    // x one K split; tiles_np = ceil(tiles_n / cl) units along the rows
+    // a unit is one weight tile x one token tile x one K split
     int tiles_n, tiles_np, tiles_m, splits, total, nk_total;
     __device__ __forceinline__ void decode(int t, int& np, int& m, int& z) const {
         np = t % tiles_np;
@@ -271,7 +270,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap0,
                  const __grid_constant__ CUtensorMap amap1, const __grid_constant__ CUtensorMap omap,
                  const __grid_constant__ CUtensorMap imap, const EpiArgs ep, int T, int R, int BN, int tmem_cols,
-                 const TileMap tm, int S, int SR, int NACC, int cl, int et) {
+                 const TileMap tm, int S, int SR, int NACC, int et) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int RAWB = KA > 1 ? Dec::template rawk<KA>() : Dec::RAW;   // raw plane bytes a stage
@@ -287,17 +286,12 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         (reinterpret_cast<uintptr_t>(bars) + sizeof(UmmaBars) + 1023) & ~uintptr_t(1023));
     float* epi_out = epi_in + (EPI_IN ? UM_EPI_IN * UM_EPI_IN_BYTES / 4 : 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // cluster of cl CTAs (1 or 2): the CTAs of a cluster take adjacent weight
-    // tiles of the same unit and share its activation tile: each loads 1/cl
-    // of it with a multicast TMA into every CTA's ring.
-    const int rank = cl > 1 ? (int)cluster_ctarank() : 0;
-    const int unit0 = blockIdx.x / cl, units = gridDim.x / cl;
-    const uint16_t cmask = (uint16_t)((1u << cl) - 1u);
+    const int unit0 = blockIdx.x, units = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < UM_STAGES; ++s) {
             mbar_init(&bars->full[s], Dec::DIRECT ? 1u : 5u);   // TMA producer (+ the stage's 4 decoder warps)
-            mbar_init(&bars->empty[s], (uint32_t)cl);     // every cluster CTA's MMA must release it
+            mbar_init(&bars->empty[s], 1u);               // the MMA warp's commit releases it
         }
         for (int r = 0; r < UM_RAW_STAGES; ++r) {
             mbar_init(&bars->raw_full[r], 1);
@@ -325,7 +319,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
-    if (cl > 1) cluster_sync();                          // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const uint32_t a_col0 = (uint32_t)(NACC * BN);       // first column of the A ring (AT)
@@ -344,7 +337,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
-                const int row0 = (np * cl + rank) * UM_BM;
+                const int row0 = np * UM_BM;
                 const int k1 = tm.kc1(z);
                 for (int kc = tm.kc0(z); kc < k1; ++kc, ++it) {
                     if (it >= S && !mbar_wait_or_abort(&bars->empty[s], ph ^ 1u, abort_flag)) {
@@ -353,16 +346,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         break;
                     }
                     mbar_arrive_expect_tx(&bars->full[s], tx);
-                    const int part = BN / cl;                  // token rows this CTA loads
-                    if (cl > 1)
-                        tma_load_2d_mc(smem + s * stage_bytes + rank * part * 128, &xmap, &bars->full[s], kc * UM_BK,
-                                       m * BN + rank * part, cmask);
-                    else {
+                    // KA atoms of BN rows, each in boxes of at most 256 rows
+                    // (the 384-token tile: three boxes of 128)
+                    const int box = BN > UM_MAX_BN ? UM_BM : BN;
 #pragma unroll
-                        for (int a = 0; a < KA; ++a)
-                            tma_load_2d(smem + s * stage_bytes + a * BN * 128, &xmap, &bars->full[s],
-                                        (kc * KA + a) * UM_BK, m * BN);
-                    }
+                    for (int a = 0; a < KA; ++a)
+                        for (int r0 = 0; r0 < BN; r0 += box)
+                            tma_load_2d(smem + s * stage_bytes + (a * BN + r0) * 128, &xmap, &bars->full[s],
+                                        (kc * KA + a) * UM_BK, m * BN + r0);
                     if (Dec::DIRECT) Dec::issue(&amap0, &amap1, a_ring + s * UM_A_STAGE, &bars->full[s], row0, kc);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
@@ -406,7 +397,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             for (int t = unit0; t < tm.total && ok && !*abort_flag; t += units) {
                 int np, m, z;
                 tm.decode(t, np, m, z);
-                const int row0 = (np * cl + rank) * UM_BM;
+                const int row0 = np * UM_BM;
                 const int k1 = tm.kc1(z);
                 for (int kc = tm.kc0(z); kc < k1; ++kc, ++it) {
                     if (it >= SR && !mbar_wait_or_abort(&bars->raw_empty[r], ph ^ 1u, abort_flag)) {
@@ -500,8 +491,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                         umma_f16_ss_elect(dcol, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j), idesc,
                                           (kc > k0 || j > 0) ? 1u : 0u);
                 }
-                if (cl > 1) umma_commit_mc_elect(&bars->empty[s], cmask);
-                else umma_commit_elect(&bars->empty[s]);
+                umma_commit_elect(&bars->empty[s]);
                 s = s1;
                 ph = ph1;
                 ready = __all_sync(0xffffffffu, ready);
@@ -609,7 +599,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         for (int t = unit0; t < tm.total; t += units, ++lt) {
             int np, m, z;
             tm.decode(t, np, m, z);
-            const int n = np * cl + rank;
+            const int n = np;
             const int buf = NACC == 2 ? (lt & 1) : 0, use = NACC == 2 ? (lt >> 1) : lt;
             if (!mbar_wait_or_abort(&bars->acc_full[buf], (uint32_t)use & 1u, abort_flag)) {
                 *abort_flag = 1;
@@ -739,9 +729,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    // every MMA of this CTA has completed (the epilogue saw each tile), so its
-    // multicast commits have landed; wait for the peers' to land here too
-    if (cl > 1) cluster_sync();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)tmem_cols);
@@ -750,31 +737,29 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 
 // Host: launch one GEMM.  act16 is f16 [T][K] (row pitch K), staged in the
 // decoder's K order; R = plane rows; splits = K splits; pm = the plane's
-// tensor maps.  Token tiles of at most 128 keep the decoded weights in
-// tensor memory (AT), and so does the 384-token wide tile; 256-token tiles
-// decode into shared memory.  Dense planes always take the shared-memory path
-// (TMA writes A).  Only the wide tile pairs CTAs on neighbouring weight tiles
-// to share its activation tile (192 rows each by multicast: a TMA box is at
-// most 256 rows); pairing at 256 tokens measured slower (a multicast tile
-// lands at about half the rate of one a CTA loads alone).
+// tensor maps.  Token tiles of at most 128, the ternary GEMM's 256-token
+// tiles and the 384-token wide tile keep the decoded weights in tensor memory
+// (AT); the blr GEMMs' 256-token tiles decode into shared memory, and dense
+// planes always take the shared-memory path (TMA writes A).  Every CTA loads
+// its own activation tile: pairs of CTAs sharing it measured slower at 256
+// tokens and the same for the wide tile.
 template <class Dec, int MODE, bool AT, int KA>
 cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void* act16, int T, int R, int K, int BN,
                              int splits, cudaStream_t st) {
     const bool wide = BN == UM_WIDE_BN;
     if ((BN > UM_MAX_BN && !wide) || BN % 16 != 0 || BN < 16 || (AT && BN > 128 && !wide && BN != UM_MAX_BN) || (wide && !AT))
         return cudaErrorInvalidValue;
-    // multi-atom stages: tensor-memory A, no clusters, every K split at least one stage
+    // multi-atom stages: tensor-memory A, every K split at least one stage
     if (KA > 1 && (!AT || wide || Dec::DIRECT || K % (UM_BK * KA) != 0 || splits > K / (UM_BK * KA)))
         return cudaErrorInvalidValue;
     // the epilogue drains 32 columns at a time: a tile narrower than a
     // multiple of 32 must be the only token tile
     if (BN % 32 != 0 && T > BN) return cudaErrorInvalidValue;
     const int tiles_n = (R + UM_BM - 1) / UM_BM;
-    const int cl = (wide && tiles_n >= 2 && BN % 32 == 0) ? 2 : 1;   // pairs share activation tiles
-    if (BN / cl > 256) return cudaErrorInvalidValue;      // a TMA box is at most 256 rows
-    CUtensorMap xmap;
+    CUtensorMap xmap;                                     // a TMA box is at most 256 rows
     if (!make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void*>(act16), (uint64_t)K,
-                            (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN / cl), CU_TENSOR_MAP_SWIZZLE_128B))
+                            (uint64_t)T, (uint64_t)K * 2, UM_BK, (uint32_t)(BN > UM_MAX_BN ? UM_BM : BN),
+                            CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // two accumulators in tensor memory (the epilogue of a tile overlaps the
     // next tile's MMAs), one for the wide tile (its epilogue, ~3 % of a
@@ -790,14 +775,14 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     // TMA epilogue (et) for the column-sum modes (without accumulation into
     // the output) of GEMMs of at most UM_EPI_TMA_STEPS 64-k steps a tile,
     // whose epilogue is not hidden behind the next tile's MMAs; needs 16-byte
-    // rows and bases, no clusters, no K split.  (Plain and scaled stores
+    // rows and bases, no K split.  (Plain and scaled stores
     // through it measured slower: the blr forward 41.8 -> 42.8 us.)
     constexpr bool EPI_IN = MODE == EPI_COLSUM || MODE == EPI_SCALE_COLSUM;
     constexpr bool EPI_OUT = MODE != EPI_COLSUM;
     const bool epi_mode = MODE == EPI_COLSUM || (MODE == EPI_SCALE_COLSUM && !ep.accumulate);
     const bool epi_aligned = ep.ldo % 4 == 0 && (!EPI_OUT || (reinterpret_cast<uintptr_t>(ep.out) & 15) == 0) &&
                              (!EPI_IN || (reinterpret_cast<uintptr_t>(ep.other) & 15) == 0);
-    int et = (epi_mode && epi_aligned && cl == 1 && splits == 1 && K / UM_BK <= UM_EPI_TMA_STEPS) ? 1 : 0;
+    int et = (epi_mode && epi_aligned && splits == 1 && K / UM_BK <= UM_EPI_TMA_STEPS) ? 1 : 0;
     int S = 0, SR = 0;
     size_t epi_bytes = 0;
     for (;; et = 0) {
@@ -835,14 +820,13 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     while (tmem_cols < NACC * BN + (AT ? S * a_cols : 0)) tmem_cols <<= 1;
     if (tmem_cols > 512) return cudaErrorInvalidValue;
     // At least 120 KB of shared memory: no two CTAs of this kernel can share
-    // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA
-    // (which a cluster barrier could otherwise turn into a deadlock).
+    // an SM, so a CTA never waits in tcgen05.alloc for a co-resident CTA.
     size_t smem = (size_t)S * (b_stage + a_stage) + (Dec::DIRECT ? 0 : (size_t)SR * raw) + 1024 + sizeof(UmmaBars) +
                   1024 + epi_bytes;
     if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
     TileMap tm;
     tm.tiles_n = tiles_n;
-    tm.tiles_np = (tiles_n + cl - 1) / cl;
+    tm.tiles_np = tiles_n;
     tm.tiles_m = (T + BN - 1) / BN;
     tm.splits = splits;
     tm.total = tm.tiles_np * tm.tiles_m * splits;
@@ -850,26 +834,22 @@ cudaError_t launch_umma_impl(const PlaneMaps& pm, const EpiArgs& ep, const void*
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int units = tm.total < sms / cl ? tm.total : sms / cl;
+    const int units = tm.total < sms ? tm.total : sms;
     cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Dec, MODE, AT, KA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * cl));
+    cfg.gridDim = dim3((unsigned)units);
     cfg.blockDim = dim3(UM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)cl;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, umma_gemm_kernel<Dec, MODE, AT, KA>, xmap, pm.m0, pm.m1, omap, imap, ep, T, R, BN,
-                              tmem_cols, tm, S, SR, NACC, cl, et);
+                              tmem_cols, tm, S, SR, NACC, et);
 }
 
 template <class Dec, int MODE>
