@@ -6,7 +6,8 @@
 // P is a packed plane (2-bit ternary codes with f16 block scales, 1-bit
 // signs) or dense f16 rows; act is an f16 activation matrix staged in the K
 // order the decoder emits pairs in.  One CTA computes a 128 (plane rows) x BN
-// (tokens) tile:
+// (tokens) tile, in pipeline stages of KA x 64 k (KA = 4 for tiles of at
+// most 128 tokens, 2 for the ternary GEMM's 256-token tiles, else 1):
 //   * one thread streams the activation tiles (B operand, 128-byte swizzle)
 //     into a ring of up to 8 stages with TMA;
 //   * a second thread streams the packed plane tiles of the same stages (the
@@ -15,16 +16,20 @@
 //     dense f16 rows skip the decoders: TMA writes them as the A operand;
 //   * eight decoder warps (one plane row per thread, two warps per 32-row
 //     quarter taking alternate stages) expand a raw stage from shared memory
-//     into the f16 A operand: into tensor memory when the token tile is at
-//     most 128 wide or the 384-token wide tile (AT), otherwise into a
-//     shared-memory ring in the MMA's K-major 128-byte-swizzled layout;
+//     into the f16 A operand: into tensor memory (AT: tiles of at most 128
+//     tokens, the ternary GEMM's 256-token tiles and the 384-token wide
+//     tile), otherwise into a shared-memory ring in the MMA's K-major
+//     128-byte-swizzled layout;
 //   * one warp issues tcgen05.mma (kind::f16, f32 accumulate in TMEM) into
-//     one of two accumulators (one for the wide tile) and frees stages with
-//     tcgen05.commit; every MMA is issued by one lane of the converged warp
-//     (elect.sync);
+//     one of two accumulators (one where A takes their room: 256 tokens with
+//     AT and the wide tile) and frees stages with tcgen05.commit; every MMA
+//     is issued by one lane of the converged warp (elect.sync);
 //   * four epilogue warps read the finished accumulator (tcgen05.ld), hand it
 //     back, and run the epilogue policy of the call while the next tile's
-//     MMAs proceed in the other accumulator.
+//     MMAs proceed in the other accumulator; for the column-sum policies of
+//     short-K GEMMs the warp that allocated tensor memory streams their
+//     operand in by TMA and the results go out by TMA store.
+// Every CTA loads its own tiles (no clusters).
 // All waits are bounded (mbar_wait); a timeout records an error and drains.
 #pragma once
 
